@@ -54,7 +54,8 @@ def _chunked(rows: int, cols: int, seed, fill, threads: int | None = None) -> np
         return out
     rpc = max(1, CHUNK_ELEMS // cols)
     starts = list(range(0, rows, rpc))
-    seeds = np.random.SeedSequence(seed).spawn(len(starts))
+    ss = seed if isinstance(seed, np.random.SeedSequence) else np.random.SeedSequence(seed)
+    seeds = ss.spawn(len(starts))
     flat = out.reshape(-1)
 
     def work(i):
