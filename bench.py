@@ -1,0 +1,432 @@
+"""Throughput of the quantize -> dequantize round trip (with the fused error statistics) on
+the large streaming workload: 32768 x 8192 bf16, |x| = exp(N(0, 2^2)) with random sign,
+to MXFP4 and to NVFP4.
+
+One step = MXFP4 quantize (+ error stats) -> dequantize (bf16), then NVFP4 amax ->
+quantize (+ error stats) -> dequantize (bf16): 5 kernel launches over inputs already in
+HBM.  The metric is GB/s of algorithmic bytes (bytes in + bytes out of every kernel of
+the step) per second of device time, and elements/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own replica on its own
+GPU (the path has no exchange step), timing is max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "quantize/dequant GB/s (bytes in+out), % of GB300 HBM peak, per format"
+ROWS, COLS = 32768, 8192
+WORKLOAD = "lognormal-stream-32768x8192-bf16"
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_SOURCES = ["precision_quantization_gb300/csrc/qz_device.cuh",
+                  "precision_quantization_gb300/csrc/qz_quant4.cu",
+                  "precision_quantization_gb300/csrc/qz_dequant.cu",
+                  "precision_quantization_gb300/csrc/qz_amax.cu"]
+
+
+def algorithmic_bytes(n: int) -> dict:
+    """Bytes in + bytes out per launch, from the formats' layouts (bf16 input and output,
+    E2M1 codes 0.5 B/element, one E8M0 byte per 32 / one E4M3 byte per 16 elements, one
+    fp32 tensor scale, one 32-byte stats record)."""
+    x = 2 * n
+    mx_out = n // 2 + n // 32
+    nv_out = n // 2 + n // 16
+    return {
+        "mx_quant": x + mx_out + 32,
+        "mx_dequant": mx_out + x,
+        "nv_amax": x + 4,
+        "nv_quant": x + 4 + nv_out + 4 + 32,
+        "nv_dequant": nv_out + 4 + x,
+    }
+
+
+def source_sha() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on this source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    k = d.get("kernels", {}).get(kernel)
+    if not k or k.get("source_sha") != source_sha():
+        return None
+    return k.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, throttle reasons) while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self) -> dict:
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[2:6]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(v: float, world: int, device) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_baseline(x_np, bytes_per_elem: float, budget_s: float = 12.0, max_rows=None) -> dict:
+    """The oracle (as it stands) on a bounded row sample of the same workload, on the host
+    cores: MXFP4 and NVFP4 quantize with stats + dequantize to bf16."""
+    import oracle as O
+    rows = 64
+    total_rows = x_np.shape[0] if max_rows is None else min(max_rows, x_np.shape[0])
+
+    def run(r):
+        sub = x_np[:r]
+        amax = O.amax(x_np)  # global amax of the whole tensor, as the GPU computes it
+        t0 = time.perf_counter()
+        for fmt in (O.MXFP4, O.NVFP4):
+            codes, sc, ts, _ = O.quantize(sub, fmt, O.GRAN_BLOCK,
+                                          tensor_amax=amax if fmt == O.NVFP4 else None,
+                                          stats=True)
+            O.dequantize(codes, sc, ts, fmt, O.GRAN_BLOCK, r, sub.shape[1], out_dtype=O.BF16)
+        return time.perf_counter() - t0
+
+    dt = run(rows)
+    while dt < budget_s / 4 and rows * 2 <= total_rows:
+        rows = min(total_rows, int(rows * max(2.0, min(8.0, budget_s / 2 / max(dt, 1e-3)))))
+        dt = run(rows)
+    n = rows * x_np.shape[1]
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    gbs = bytes_per_elem * n / dt / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {rows} rows x {x_np.shape[1]} of the workload ({n} elements), "
+                      f"MXFP4+NVFP4 quantize(+stats)->dequantize, {dt:.2f} s",
+            "elements_per_s": round(n / dt, 1)}
+
+
+def run_reference(args, world, rank):
+    """The CPU oracle timed as the reference arm, on bounded samples of the workload."""
+    if rank != 0:
+        return
+    import numpy as np
+    import workloads as W
+    import oracle as O
+    x = W.workload(4)
+    n = ROWS * COLS
+    bpe = sum(algorithmic_bytes(n).values()) / n
+    sample_rows = 256
+    amax = O.amax(x)
+
+    def step():
+        sub = x[:sample_rows]
+        for fmt in (O.MXFP4, O.NVFP4):
+            codes, sc, ts, _ = O.quantize(sub, fmt, O.GRAN_BLOCK,
+                                          tensor_amax=amax if fmt == O.NVFP4 else None,
+                                          stats=True)
+            O.dequantize(codes, sc, ts, fmt, O.GRAN_BLOCK, sample_rows, COLS, out_dtype=O.BF16)
+
+    for _ in range(args.warmup):
+        step()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        step()
+        times.append(time.perf_counter() - t0)
+    dt = statistics.mean(times)
+    ne = sample_rows * COLS
+    value = bpe * ne / dt / 1e9
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "rows": ROWS, "cols": COLS,
+                   "formats": ["mxfp4", "nvfp4"], "sample_rows_per_step": sample_rows},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"first {sample_rows} rows x {COLS} per step ({ne} elements)"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "elements_per_s": round(ne / dt, 1),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world, rank, local = dist_setup()
+
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import numpy as np
+    import torch
+    import precision_quantization_gb300 as qz
+    import workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    x_np = W.workload(4)
+    n = ROWS * COLS
+    x = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16).to(dev)
+    ws = qz.Workspace(dev)
+    outs = {f: qz.alloc_outputs(f, qz.QZ_GRAN_BLOCK, ROWS, COLS, dev)
+            for f in (qz.QZ_MXFP4, qz.QZ_NVFP4)}
+    ys = {f: torch.empty((ROWS, COLS), dtype=torch.bfloat16, device=dev) for f in outs}
+    sts = {f: torch.empty((qz.STATS_BYTES,), dtype=torch.uint8, device=dev) for f in outs}
+    amax_buf = torch.empty((1,), dtype=torch.float32, device=dev)
+    flush = torch.empty((L2_FLUSH_BYTES,), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sptr = stream.cuda_stream
+    desc = {f: qz.make_desc(f, qz.QZ_BF16, qz.QZ_GRAN_BLOCK, ROWS, COLS) for f in outs}
+    desc_amax = qz.make_desc(qz.QZ_INT8, qz.QZ_BF16, qz.QZ_GRAN_TENSOR, ROWS, COLS)
+    names = ["mx_quant", "mx_dequant", "nv_amax", "nv_quant", "nv_dequant"]
+    abytes = algorithmic_bytes(n)
+    step_bytes = sum(abytes.values())
+
+    def launches(x_ptr, ev=None):
+        """The 5 launches of one step; ev: optional list of 6 events bracketing them."""
+        def mark(i):
+            if ev is not None:
+                ev[i].record(stream)
+        mark(0)
+        c, s, t = outs[qz.QZ_MXFP4]
+        rc = qz.qz_quantize(desc[qz.QZ_MXFP4], x_ptr, c.data_ptr(), s.data_ptr(), t.data_ptr(),
+                            None, sts[qz.QZ_MXFP4].data_ptr(), ws.ptr, sptr)
+        mark(1)
+        rc |= qz.qz_dequantize(desc[qz.QZ_MXFP4], c.data_ptr(), s.data_ptr(), t.data_ptr(),
+                               ys[qz.QZ_MXFP4].data_ptr(), qz.QZ_BF16, sptr)
+        mark(2)
+        rc |= qz.qz_amax(desc_amax, x_ptr, amax_buf.data_ptr(), ws.ptr, sptr)
+        mark(3)
+        c, s, t = outs[qz.QZ_NVFP4]
+        rc |= qz.qz_quantize(desc[qz.QZ_NVFP4], x_ptr, c.data_ptr(), s.data_ptr(), t.data_ptr(),
+                             amax_buf.data_ptr(), sts[qz.QZ_NVFP4].data_ptr(), ws.ptr, sptr)
+        mark(4)
+        rc |= qz.qz_dequantize(desc[qz.QZ_NVFP4], c.data_ptr(), s.data_ptr(), t.data_ptr(),
+                               ys[qz.QZ_NVFP4].data_ptr(), qz.QZ_BF16, sptr)
+        mark(5)
+        if rc != 0:
+            raise RuntimeError(f"libqz call failed ({rc})")
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        launches(x.data_ptr())
+    torch.cuda.synchronize(dev)
+    if ws.status() != 0:
+        raise RuntimeError("non-finite input flagged")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        for k in range(args.steps):
+            flush.zero_()  # L2 flush between timed steps (outside the events)
+            launches(x.data_ptr(), evs[k])
+        torch.cuda.synchronize(dev)
+        wall = time.perf_counter() - t0
+    if world > 1:
+        torch.distributed.barrier()
+    per_kernel = {nm: [] for nm in names}
+    step_ms = []
+    for ev in evs:
+        step_ms.append(ev[0].elapsed_time(ev[5]))
+        for i, nm in enumerate(names):
+            per_kernel[nm].append(ev[i].elapsed_time(ev[i + 1]))
+    ms = statistics.mean(step_ms)
+    ms = max_over_ranks(ms, world, dev)
+    value = step_bytes * world / (ms * 1e-3) / 1e9
+    peaks = measured_peaks()
+    kern = {}
+    for nm in names:
+        avg = statistics.mean(per_kernel[nm])
+        kern[nm] = {"ms": round(avg, 5), "gbs": round(abytes[nm] / (avg * 1e-3) / 1e9, 1),
+                    "frac_hbm": round(abytes[nm] / (avg * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}
+    dominant = max(names, key=lambda nm: kern[nm]["ms"])
+    achieved = abytes[dominant] / (kern[dominant]["ms"] * 1e-3) / 1e9
+    stats_host = {f: qz.read_stats(sts[f]) for f in outs}
+
+    # ---- end to end through the public API: pinned host input in, quantized tensors out
+    e2e = None
+    if not args.no_e2e:
+        xh = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16).pin_memory()
+        host_out = {f: [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs[f]] +
+                    [torch.empty((qz.STATS_BYTES,), dtype=torch.uint8).pin_memory()]
+                    for f in outs}
+        xd = torch.empty_like(x)
+        h2d = xh.numel() * 2
+        d2h = sum(t.numel() * t.element_size() for f in outs for t in host_out[f])
+
+        def e2e_step():
+            xd.copy_(xh, non_blocking=True)
+            launches(xd.data_ptr())
+            for f in outs:
+                for hsrc, hdst in zip(list(outs[f]) + [sts[f]], host_out[f]):
+                    hdst.copy_(hsrc, non_blocking=True)
+            torch.cuda.synchronize(dev)
+
+        for _ in range(2):
+            e2e_step()
+        e_ms = []
+        for _ in range(args.e2e_steps):
+            flush.zero_()
+            torch.cuda.synchronize(dev)
+            t1 = time.perf_counter()
+            e2e_step()
+            e_ms.append((time.perf_counter() - t1) * 1e3)
+        em = max_over_ranks(statistics.mean(e_ms), world, dev)
+        e2e = {"value": round(step_bytes * world / (em * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(em, 3)}
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = cpu_baseline(x_np, step_bytes / n)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "rows": ROWS, "cols": COLS, "input": "bf16",
+                   "formats": ["mxfp4", "nvfp4"],
+                   "step": "mx quantize(+stats)->dequantize(bf16); nv amax->quantize(+stats)"
+                           "->dequantize(bf16)",
+                   "bytes_per_step": step_bytes,
+                   "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write); "
+                         "input 512 MiB > L2",
+                   "parallelism": f"replicas x{world}"},
+        "elements_per_s": round(n * 2 * world / (ms * 1e-3), 1),
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1),
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "peak_source": peaks["source"], "traffic": recorded_traffic(dominant),
+                     "algorithmic_bytes_per_launch": abytes[dominant]},
+        "kernels": kern,
+        "per_format": {
+            "mxfp4": {"round_trip_gbs": round((abytes["mx_quant"] + abytes["mx_dequant"]) /
+                      ((kern["mx_quant"]["ms"] + kern["mx_dequant"]["ms"]) * 1e-3) / 1e9, 1),
+                      "mse": stats_host[qz.QZ_MXFP4].mse,
+                      "max_rel_err": stats_host[qz.QZ_MXFP4].max_rel_err},
+            "nvfp4": {"round_trip_gbs": round((abytes["nv_amax"] + abytes["nv_quant"] +
+                      abytes["nv_dequant"]) / ((kern["nv_amax"]["ms"] + kern["nv_quant"]["ms"] +
+                      kern["nv_dequant"]["ms"]) * 1e-3) / 1e9, 1),
+                      "mse": stats_host[qz.QZ_NVFP4].mse,
+                      "max_rel_err": stats_host[qz.QZ_NVFP4].max_rel_err},
+        },
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps * len(names),
+        "clocks": clk.summary(),
+        "wall_s_timed_region": round(wall, 4),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+/*
+ * qz.h -- C ABI of libqz: quantize a 2-D tensor on a GB300 (sm_103a) GPU to symmetric INT8,
+ * FP8 E4M3 / E5M2, MXFP4 or NVFP4, dequantize it again, and reduce the quantization error.
+ *
+ * The operations are the ones defined in the blog post "浅谈低精度浮点数" ("A brief talk
+ * on low-precision floats", july-h5kf3.github.io column blog):
+ *   - section "FP8": symmetric INT8, x^ = s * round(x / s), q in [-127, 127],
+ *     s = alpha / 127 with alpha the largest magnitude; FP8 E4M3 and E5M2;
+ *   - section "FP4 / MXFP4 / NVFP4": the E2M1 element values {0, 0.5, 1, 1.5, 2, 3, 4, 6},
+ *     MXFP4 (32 values share one power-of-two E8M0 scale, s = 2^round(log2(A/6)), rounded
+ *     up in practice), NVFP4 (16 values share one E4M3 scale, times one fp32 per-tensor
+ *     scale: s_global = global_amax / (6 * 448), s_block = (block_amax / 6) / s_global,
+ *     x^ = s_global * s_block * Q_E2M1(x / (s_global * s_block)));
+ *   - the error measures discussed there: |x - x^| and |x - x^| / |x|.
+ * Packing of two FP4 codes per byte follows the "Puzzles 12 Quantized Matrix Mult" section
+ * of the same blog's "Triton" post: element j of a packed word sits in bits [4j, 4j+4), so
+ * the first element of a pair is the low nibble.
+ *
+ * Exact semantics (every result is bit-exact, error statistics aside):
+ *   element step   v = fl32(x / s)  (IEEE binary32 division), then round to the nearest
+ *                  grid value, ties to the code with an even last bit; values at or beyond
+ *                  the format maximum saturate (INT8 127, E4M3 448, E5M2 57344, E2M1 6);
+ *                  FP formats keep the sign of zero, INT8 has one zero (-128 never occurs).
+ *   INT8 / FP8     s = fl32(alpha / qmax) with qmax = 127, 448 or 57344; alpha is the
+ *                  largest |x| of the tensor (TENSOR) or of the row (ROW); s = 1 when that
+ *                  quotient is 0.  UNIT uses s = 1.
+ *   MXFP4          per 32-element block with largest magnitude A: t = fl32(A / 6);
+ *                  k = smallest integer with 2^k >= t (QZ_SCALE_UP) or k = round(log2 t)
+ *                  (QZ_SCALE_NEAREST), clamped to [-127, 127], k = -127 when t = 0;
+ *                  scale code (E8M0, bias 127) = k + 127; v = x * 2^-k (exact).
+ *                  UNIT uses k = 0.
+ *   NVFP4          s_g = fl32(alpha / 2688) (1 when 0); per 16-element block
+ *                  t = fl32(fl32(A / 6) / s_g); block code = smallest E4M3 value >= t,
+ *                  saturated at 448 (QZ_SCALE_UP) or RNE-saturating E4M3 (QZ_SCALE_NEAREST);
+ *                  s = fl32(s_g * decode(block code)); s = 0 gives signed-zero codes.
+ *                  UNIT uses s_g = 1 and block code 0x38 (1.0).
+ *   dequantize     x^ = fl32(decode(q) * s), then converted to the output dtype (bf16 by
+ *                  round-to-nearest-even, or fp32 as is).
+ *   stats          e = fl32(x - x^) with the fp32 x^; sum_sq_err = sum e^2; mse =
+ *                  sum_sq_err / n; max_abs_err = max |e| (exact); max_rel_err = max over
+ *                  x != 0 of fl32(|e| / |x|) (exact).  sum_sq_err / mse are accumulated
+ *                  with compensated fp32 per thread and fp64 across threads: relative
+ *                  error below 1e-5.
+ *
+ * Layouts.  The high-precision tensor (x for quantize / stats, y for dequantize) is
+ * [rows, cols] row-major with leading dimension ld >= cols, in elements.  Everything else
+ * is dense row-major:
+ *   codes   INT8 / FP8: rows * cols bytes; MXFP4 / NVFP4: rows * cols / 2 bytes.
+ *   scales  ROW: rows fp32; MXFP4: rows * cols / 32 E8M0 bytes; NVFP4: rows * cols / 16
+ *           E4M3 bytes; otherwise unused (may be NULL).
+ *   tensor_scale  one fp32: s for TENSOR, s_g for NVFP4 BLOCK, 1 for UNIT.
+ * Blocks run along cols.  MXFP4 needs cols % 32 == 0, NVFP4 cols % 16 == 0.
+ *
+ * Ownership and concurrency.  The caller allocates every buffer (all device memory except
+ * the host pointer of qz_get_device_status).  The library allocates nothing and keeps no
+ * global state.  Every call is asynchronous on `stream` (NULL = the legacy default
+ * stream); argument errors are returned synchronously, before anything is enqueued.
+ * Calls that share one workspace must be ordered on one stream.
+ *
+ * Alignment.  Pointers need only the natural alignment of their element type.  Fast
+ * vectorised kernels are used when x / y and ld allow 16-byte (INT8 / FP8) or 32-byte
+ * (MXFP4 / NVFP4) row access and codes are 16-byte aligned; other shapes run element-wise
+ * kernels with the same results.
+ *
+ * Non-finite inputs (NaN, +-Inf) are outside the contract: the codes are unspecified and
+ * bit 0 of the workspace status word is set (read it with qz_get_device_status).
+ */
+#ifndef QZ_H
+#define QZ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define QZ_API __attribute__((visibility("default")))
+#else
+#define QZ_API
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* qz_stream_t;
+
+typedef enum {
+  QZ_OK = 0,
+  QZ_ERR_NULL = 1,        /* a required pointer is NULL                                */
+  QZ_ERR_ENUM = 2,        /* a descriptor field holds an unknown enumerator            */
+  QZ_ERR_SHAPE = 3,       /* rows / cols / ld out of range, or cols % block_size != 0  */
+  QZ_ERR_ALIGN = 4,       /* a pointer lacks the natural alignment of its element type */
+  QZ_ERR_UNSUPPORTED = 5, /* a valid but unsupported combination (format x granularity) */
+  QZ_ERR_CUDA = 6,        /* a kernel launch failed                                    */
+  QZ_ERR_WORKSPACE = 7    /* workspace missing or smaller than qz_workspace_size()     */
+} qz_status;
+
+typedef enum { QZ_INT8 = 1, QZ_FP8_E4M3 = 2, QZ_FP8_E5M2 = 3, QZ_MXFP4 = 4, QZ_NVFP4 = 5 } qz_format;
+typedef enum { QZ_BF16 = 1, QZ_F32 = 2 } qz_dtype;
+typedef enum {
+  QZ_GRAN_TENSOR = 1, /* one scale for the tensor (INT8 / FP8)                     */
+  QZ_GRAN_ROW = 2,    /* one scale per row: per output channel / per token (INT8/FP8) */
+  QZ_GRAN_BLOCK = 3,  /* per block along cols (MXFP4 32, NVFP4 16)                 */
+  QZ_GRAN_UNIT = 4    /* scale 1: the bare element cast (all formats)              */
+} qz_granularity;
+typedef enum { QZ_ROUND_RNE = 0 } qz_elem_round;
+typedef enum { QZ_SCALE_UP = 0, QZ_SCALE_NEAREST = 1 } qz_scale_round;
+
+/* Status-word bits (qz_get_device_status). */
+#define QZ_FLAG_NONFINITE_INPUT 0x1u /* a NaN or Inf element was read                   */
+#define QZ_FLAG_BAD_AMAX 0x2u        /* a caller-supplied tensor amax was < 0 or NaN     */
+
+typedef struct {
+  int32_t format;      /* qz_format                                                  */
+  int32_t in_dtype;    /* qz_dtype of x (quantize, stats, amax)                      */
+  int32_t granularity; /* qz_granularity                                             */
+  int32_t block_size;  /* 32 for MXFP4, 16 for NVFP4, 0 for INT8 / FP8               */
+  int32_t elem_round;  /* QZ_ROUND_RNE                                               */
+  int32_t scale_round; /* qz_scale_round (MXFP4 / NVFP4 BLOCK)                       */
+  int64_t rows;        /* >= 0                                                       */
+  int64_t cols;        /* >= 0                                                       */
+  int64_t ld;          /* leading dimension of x / y in elements, >= cols            */
+} qz_desc;
+
+/* Error statistics, written to device memory by qz_quantize / qz_error_stats. */
+typedef struct {
+  double sum_sq_err;
+  double mse;
+  float max_rel_err;
+  float max_abs_err;
+  uint64_t n;
+} qz_stats;
+
+/* Human-readable name of a status code (static storage). */
+QZ_API const char* qz_status_string(qz_status status);
+
+/* Bytes of device workspace the calls below need for this descriptor (the same for every
+ * descriptor of this library version).  The workspace must be zeroed once before its first
+ * use (qz_workspace_init); the calls leave it ready for the next call. */
+QZ_API size_t qz_workspace_size(const qz_desc* desc);
+
+/* Zero `bytes` of workspace on `stream`. */
+QZ_API qz_status qz_workspace_init(void* ws, size_t bytes, qz_stream_t stream);
+
+/* Largest |x| of the tensor into *amax_dev (device fp32).  Sets QZ_FLAG_NONFINITE_INPUT
+ * when a NaN / Inf is read.  Needs the workspace. */
+QZ_API qz_status qz_amax(const qz_desc* desc, const void* x, float* amax_dev, void* ws,
+                  qz_stream_t stream);
+
+/* Quantize x into codes (+ scales, + tensor_scale_dev).
+ *   tensor_amax_dev  optional device fp32: the alpha of TENSOR / NVFP4 BLOCK (the post
+ *                    leaves open where NVFP4's global amax comes from); NULL = computed
+ *                    here with an extra read of x.  Must be finite and >= 0.
+ *   tensor_scale_dev written (one fp32) when non-NULL; required for TENSOR and NVFP4 BLOCK.
+ *   stats_dev        optional: the error statistics of this quantization, fused into the
+ *                    same pass (no extra read of x).
+ *   ws               workspace (qz_workspace_size bytes); required when the amax is
+ *                    computed or stats_dev is non-NULL, may be NULL otherwise. */
+QZ_API qz_status qz_quantize(const qz_desc* desc, const void* x, void* codes, void* scales,
+                      float* tensor_scale_dev, const float* tensor_amax_dev,
+                      qz_stats* stats_dev, void* ws, qz_stream_t stream);
+
+/* Dequantize codes (+ scales, + tensor_scale_dev) into y ([rows, cols], leading dimension
+ * desc->ld) of dtype out_dtype.  desc->in_dtype is ignored. */
+QZ_API qz_status qz_dequantize(const qz_desc* desc, const void* codes, const void* scales,
+                        const float* tensor_scale_dev, void* y, int32_t out_dtype,
+                        qz_stream_t stream);
+
+/* Error statistics of existing codes against x, without writing anything but stats_dev. */
+QZ_API qz_status qz_error_stats(const qz_desc* desc, const void* x, const void* codes,
+                         const void* scales, const float* tensor_scale_dev,
+                         qz_stats* stats_dev, void* ws, qz_stream_t stream);
+
+/* Synchronize `stream`, then copy the workspace status word (QZ_FLAG_* bits, sticky until
+ * qz_workspace_init) into *flags_host. */
+QZ_API qz_status qz_get_device_status(const void* ws, uint32_t* flags_host, qz_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QZ_H */

@@ -1,0 +1,51 @@
+// qz_internal.h -- host-side plumbing shared by the translation units of libqz.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "qz.h"
+
+namespace qz {
+
+// Geometry of one launch over a [rows, cols] high-precision tensor cut into 32-byte
+// chunks along each row.
+struct Geom {
+  int64_t rows = 0, cols = 0, ld = 0;
+  int64_t cpr = 0;       // chunks per row (ceil(cols / elements-per-chunk))
+  int64_t n_chunks = 0;  // rows * cpr
+  bool dense = false;    // ld == cols: a chunk's address is base + 32 * index
+  bool vec = false;      // 32-byte vector access is legal (alignment + full chunks)
+};
+
+Geom make_geom(const qz_desc& d, const void* hp, int elem_bytes, int align_bytes);
+
+// Persistent-grid size: resident CTAs of `kernel` on every SM, capped by the work and by
+// the partial-result slots of the workspace.
+int grid_for(const void* kernel, int64_t work_ctas, cudaStream_t stream);
+
+qz_status launch_amax(const qz_desc& d, const void* x, float* out, void* ws, cudaStream_t s);
+
+qz_status launch_quant8(const qz_desc& d, const void* x, void* codes, void* scales,
+                        float* tscale_out, const float* amax, bool amax_supplied,
+                        qz_stats* stats, void* ws, cudaStream_t s);
+qz_status launch_quant4(const qz_desc& d, const void* x, void* codes, void* scales,
+                        float* tscale_out, const float* amax, bool amax_supplied,
+                        qz_stats* stats, void* ws, cudaStream_t s);
+qz_status launch_dequant8(const qz_desc& d, const void* codes, const void* scales,
+                          const float* tscale, void* y, int out_dtype, cudaStream_t s);
+qz_status launch_dequant4(const qz_desc& d, const void* codes, const void* scales,
+                          const float* tscale, void* y, int out_dtype, cudaStream_t s);
+qz_status launch_stats8(const qz_desc& d, const void* x, const void* codes,
+                        const void* scales, const float* tscale, qz_stats* stats, void* ws,
+                        cudaStream_t s);
+qz_status launch_stats4(const qz_desc& d, const void* x, const void* codes,
+                        const void* scales, const float* tscale, qz_stats* stats, void* ws,
+                        cudaStream_t s);
+qz_status launch_empty(float* tscale_out, qz_stats* stats, cudaStream_t s);
+
+inline qz_status launch_status() {
+  return cudaGetLastError() == cudaSuccess ? QZ_OK : QZ_ERR_CUDA;
+}
+
+}  // namespace qz

@@ -1,0 +1,146 @@
+"""The C ABI of libqz without a GPU: the library loads, exports every function that
+include/qz.h declares, its structs have the header's layout, and argument errors come
+back synchronously (they are checked before any CUDA call)."""
+import ctypes as C
+import os
+import re
+import subprocess
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "qz.h")
+
+
+@pytest.fixture(scope="module")
+def qz():
+    import __graft_entry__
+    __graft_entry__.build_library()
+    import precision_quantization_gb300 as qz
+    qz.lib()
+    return qz
+
+
+def declared_functions():
+    txt = open(HEADER, encoding="utf-8").read()
+    return set(re.findall(r"QZ_API\s+[\w\s\*]+?\b(qz_\w+)\s*\(", txt))
+
+
+def test_exports_every_declared_symbol(qz):
+    decl = declared_functions()
+    assert decl == set(qz.ABI_SYMBOLS)
+    out = subprocess.run(["nm", "-D", "--defined-only", qz.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if ln.strip()}
+    assert decl <= exported
+    for name in decl:
+        assert hasattr(qz.lib(), name)
+
+
+def test_struct_layout_matches_header(qz, tmp_path):
+    src = tmp_path / "layout.c"
+    src.write_text(
+        '#include <stdio.h>\n#include <stddef.h>\n#include "qz.h"\n'
+        "int main(void){printf(\"%zu %zu %zu %zu %zu %zu %zu %zu\\n\","
+        " sizeof(qz_desc), offsetof(qz_desc, rows), offsetof(qz_desc, ld),"
+        " sizeof(qz_stats), offsetof(qz_stats, mse), offsetof(qz_stats, max_rel_err),"
+        " offsetof(qz_stats, max_abs_err), offsetof(qz_stats, n)); return 0;}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)],
+                   check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    want = [C.sizeof(qz.QzDesc), qz.QzDesc.rows.offset, qz.QzDesc.ld.offset,
+            C.sizeof(qz.QzStats), qz.QzStats.mse.offset, qz.QzStats.max_rel_err.offset,
+            qz.QzStats.max_abs_err.offset, qz.QzStats.n.offset]
+    assert got == want
+
+
+def test_enum_values_match_header(qz):
+    txt = open(HEADER, encoding="utf-8").read()
+    for name, val in re.findall(r"\b(QZ_[A-Z0-9_]+)\s*=\s*(\d+)", txt):
+        assert getattr(qz, name) == int(val), name
+    for name, val in re.findall(r"#define\s+(QZ_FLAG_\w+)\s+(0x[0-9a-fA-F]+)u", txt):
+        assert getattr(qz, name) == int(val, 16)
+
+
+def test_status_strings(qz):
+    for s in range(8):
+        assert qz.qz_status_string(s) and qz.qz_status_string(s) != "unknown status"
+    assert qz.qz_status_string(99) == "unknown status"
+
+
+def test_workspace_size(qz):
+    n = qz.qz_workspace_size()
+    assert n >= 256 and n % 16 == 0
+    d = qz.make_desc("nvfp4", qz.QZ_BF16, "block", 128, 256)
+    assert qz.qz_workspace_size(d) == n
+
+
+FAKE = 1 << 20  # never dereferenced: every call below fails validation first
+
+
+@pytest.mark.parametrize("mutate,want", [
+    (lambda d: setattr(d, "format", 9), "QZ_ERR_ENUM"),
+    (lambda d: setattr(d, "granularity", 0), "QZ_ERR_ENUM"),
+    (lambda d: setattr(d, "elem_round", 1), "QZ_ERR_ENUM"),
+    (lambda d: setattr(d, "scale_round", 2), "QZ_ERR_ENUM"),
+    (lambda d: setattr(d, "in_dtype", 7), "QZ_ERR_ENUM"),
+    (lambda d: setattr(d, "rows", -1), "QZ_ERR_SHAPE"),
+    (lambda d: setattr(d, "ld", 10), "QZ_ERR_SHAPE"),
+    (lambda d: setattr(d, "cols", 40), "QZ_ERR_SHAPE"),         # not a multiple of 16
+    (lambda d: setattr(d, "block_size", 32), "QZ_ERR_UNSUPPORTED"),
+    (lambda d: setattr(d, "granularity", 2), "QZ_ERR_UNSUPPORTED"),  # NVFP4 per row
+])
+def test_quantize_argument_errors(qz, mutate, want):
+    d = qz.make_desc("nvfp4", qz.QZ_BF16, "block", 4, 64)
+    mutate(d)
+    rc = qz.qz_quantize(d, FAKE, FAKE, FAKE, FAKE, FAKE, None, None)
+    assert rc == getattr(qz, want)
+
+
+def test_quantize_null_and_workspace_errors(qz):
+    assert qz.lib().qz_quantize(None, FAKE, FAKE, FAKE, FAKE, None, None, None, None) == qz.QZ_ERR_NULL
+    d = qz.make_desc("e4m3", qz.QZ_BF16, "tensor", 4, 64)
+    # per-tensor scale computed in the library: needs a workspace
+    assert qz.qz_quantize(d, FAKE, FAKE, None, FAKE, None, None, None) == qz.QZ_ERR_WORKSPACE
+    # ... and a tensor-scale output
+    assert qz.qz_quantize(d, FAKE, FAKE, None, None, FAKE, None, None) == qz.QZ_ERR_NULL
+    # misaligned workspace / stats
+    assert qz.qz_quantize(d, FAKE, FAKE, None, FAKE, None, None, FAKE + 4) == qz.QZ_ERR_ALIGN
+    assert qz.qz_quantize(d, FAKE, FAKE, None, FAKE, FAKE, FAKE + 4, FAKE) == qz.QZ_ERR_ALIGN
+    # missing x / codes / row scales
+    d_row = qz.make_desc("int8", qz.QZ_F32, "row", 4, 64)
+    assert qz.qz_quantize(d_row, None, FAKE, FAKE, None, None, None, None) == qz.QZ_ERR_NULL
+    assert qz.qz_quantize(d_row, FAKE, FAKE, None, None, None, None, None) == qz.QZ_ERR_NULL
+    # misaligned fp32 input
+    assert qz.qz_quantize(d_row, FAKE + 2, FAKE, FAKE, None, None, None, None) == qz.QZ_ERR_ALIGN
+    # 8-bit formats take no block size and no BLOCK granularity
+    d_bad = qz.make_desc("int8", qz.QZ_F32, "block", 4, 64)
+    assert qz.qz_quantize(d_bad, FAKE, FAKE, FAKE, FAKE, None, None, FAKE) == qz.QZ_ERR_UNSUPPORTED
+
+
+def test_dequantize_and_stats_argument_errors(qz):
+    d = qz.make_desc("mxfp4", qz.QZ_BF16, "block", 4, 64)
+    assert qz.qz_dequantize(d, FAKE, FAKE, None, FAKE, 5) == qz.QZ_ERR_ENUM
+    assert qz.qz_dequantize(d, None, FAKE, None, FAKE, qz.QZ_BF16) == qz.QZ_ERR_NULL
+    assert qz.qz_dequantize(d, FAKE, None, None, FAKE, qz.QZ_BF16) == qz.QZ_ERR_NULL
+    assert qz.qz_dequantize(d, FAKE, FAKE, None, FAKE + 1, qz.QZ_BF16) == qz.QZ_ERR_ALIGN
+    dn = qz.make_desc("nvfp4", qz.QZ_BF16, "block", 4, 64)
+    assert qz.qz_dequantize(dn, FAKE, FAKE, None, FAKE, qz.QZ_F32) == qz.QZ_ERR_NULL
+    assert qz.qz_error_stats(d, FAKE, FAKE, FAKE, None, None, FAKE) == qz.QZ_ERR_NULL
+    assert qz.qz_error_stats(d, FAKE, FAKE, FAKE, None, FAKE, None) == qz.QZ_ERR_WORKSPACE
+    assert qz.qz_amax(d, FAKE, None, FAKE) == qz.QZ_ERR_NULL
+    assert qz.qz_workspace_init(None, 1 << 20) == qz.QZ_ERR_NULL
+    assert qz.qz_workspace_init(FAKE, 16) == qz.QZ_ERR_WORKSPACE
+    st, _ = qz.qz_get_device_status(None)
+    assert st == qz.QZ_ERR_NULL
+
+
+def test_binding_fails_loudly_without_library(qz, monkeypatch, tmp_path):
+    import precision_quantization_gb300 as mod
+    monkeypatch.setattr(mod, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(mod, "_lib", None)
+    with pytest.raises(ImportError):
+        mod.lib()
