@@ -99,7 +99,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -109,7 +109,15 @@ class ClockSampler:
 
     def _read(self):
         for ln in self.proc.stdout:
-            self.lines.append(ln.strip())
+            self.lines.append((time.perf_counter(), ln.strip()))
+
+    def wait_first(self, timeout: float = 10.0):
+        t = time.perf_counter()
+        while self.proc and not self.lines and time.perf_counter() - t < timeout:
+            time.sleep(0.02)
+
+    def window(self, t0: float, t1: float):
+        self.t0, self.t1 = t0, t1
 
     def __exit__(self, *a):
         if self.proc:
@@ -123,7 +131,11 @@ class ClockSampler:
     def summary(self) -> dict:
         sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        t0, t1 = getattr(self, "t0", None), getattr(self, "t1", None)
+        sel = [ln for (ts, ln) in self.lines if t0 is None or t0 <= ts <= t1 + 0.25]
+        if not sel and self.lines:  # region shorter than the sampling period: nearest sample
+            sel = [min(self.lines, key=lambda p: abs(p[0] - (t0 or 0)))[1]]
+        for ln in sel:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 6:
                 continue
@@ -239,12 +251,14 @@ def run_reference(args, world, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--rows", type=int, default=ROWS,
+                    help="rows of the workload (same recipe); the default is the full size")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world, rank, local = dist_setup()
@@ -264,20 +278,21 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    x_np = W.workload(4)
-    n = ROWS * COLS
+    rows = args.rows
+    x_np = W.workload(4, rows=rows)
+    n = rows * COLS
     x = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16).to(dev)
     ws = qz.Workspace(dev)
-    outs = {f: qz.alloc_outputs(f, qz.QZ_GRAN_BLOCK, ROWS, COLS, dev)
+    outs = {f: qz.alloc_outputs(f, qz.QZ_GRAN_BLOCK, rows, COLS, dev)
             for f in (qz.QZ_MXFP4, qz.QZ_NVFP4)}
-    ys = {f: torch.empty((ROWS, COLS), dtype=torch.bfloat16, device=dev) for f in outs}
+    ys = {f: torch.empty((rows, COLS), dtype=torch.bfloat16, device=dev) for f in outs}
     sts = {f: torch.empty((qz.STATS_BYTES,), dtype=torch.uint8, device=dev) for f in outs}
     amax_buf = torch.empty((1,), dtype=torch.float32, device=dev)
     flush = torch.empty((L2_FLUSH_BYTES,), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
-    desc = {f: qz.make_desc(f, qz.QZ_BF16, qz.QZ_GRAN_BLOCK, ROWS, COLS) for f in outs}
-    desc_amax = qz.make_desc(qz.QZ_INT8, qz.QZ_BF16, qz.QZ_GRAN_TENSOR, ROWS, COLS)
+    desc = {f: qz.make_desc(f, qz.QZ_BF16, qz.QZ_GRAN_BLOCK, rows, COLS) for f in outs}
+    desc_amax = qz.make_desc(qz.QZ_INT8, qz.QZ_BF16, qz.QZ_GRAN_TENSOR, rows, COLS)
     names = ["mx_quant", "mx_dequant", "nv_amax", "nv_quant", "nv_dequant"]
     abytes = algorithmic_bytes(n)
     step_bytes = sum(abytes.values())
@@ -307,24 +322,27 @@ def main():
         if rc != 0:
             raise RuntimeError(f"libqz call failed ({rc})")
 
+    clk = ClockSampler(local).__enter__()
     for _ in range(args.warmup):
         flush.zero_()
         launches(x.data_ptr())
     torch.cuda.synchronize(dev)
     if ws.status() != 0:
         raise RuntimeError("non-finite input flagged")
+    clk.wait_first()
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clk:
-        t0 = time.perf_counter()
-        for k in range(args.steps):
-            flush.zero_()  # L2 flush between timed steps (outside the events)
-            launches(x.data_ptr(), evs[k])
-        torch.cuda.synchronize(dev)
-        wall = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.zero_()  # L2 flush between timed steps (outside the events)
+        launches(x.data_ptr(), evs[k])
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t0
+    clk.window(t0, t0 + wall)
+    clk.__exit__()
     if world > 1:
         torch.distributed.barrier()
     per_kernel = {nm: [] for nm in names}
@@ -391,7 +409,8 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "rows": ROWS, "cols": COLS, "input": "bf16",
+        "config": {"workload": WORKLOAD if rows == ROWS else f"{WORKLOAD} (first {rows} rows)",
+                   "rows": rows, "cols": COLS, "input": "bf16",
                    "formats": ["mxfp4", "nvfp4"],
                    "step": "mx quantize(+stats)->dequantize(bf16); nv amax->quantize(+stats)"
                            "->dequantize(bf16)",

@@ -146,10 +146,12 @@ __device__ __forceinline__ bool is_finite_f(float a) { return fabsf(a) <= 3.4028
 // RN(q + r*y) is the correctly rounded quotient).  Exact when s, 1/s and the quotient are
 // normal binary32 numbers and x is not tiny; callers guard the ranges where that fails
 // (fast_div_ok) and use __fdiv_rn there.
+// The quotient of x by s > 0 has the sign of x; the correction step alone would turn
+// x = -0 into +0 (fma(+0, r, -0) = +0), so the sign is copied from x.
 __device__ __forceinline__ float div_by(float x, float s, float r) {
   const float q = __fmul_rn(x, r);
   const float rem = __fmaf_rn(-q, s, x);
-  return __fmaf_rn(rem, r, q);
+  return copysignf(__fmaf_rn(rem, r, q), x);
 }
 
 // Range in which div_by is exact for every quotient that can change a code: s in
@@ -301,7 +303,8 @@ __device__ __forceinline__ uint32_t nv_block_code(float t, int scale_round) {
 // rare candidates get an exact __fdiv_rn.  No ratio exceeds 1 (0 is a grid value, so the
 // nearest code is never farther from x than 0 is), so once T == 1 the test is skipped.
 struct StatAcc {
-  float s = 0.0f, c = 0.0f;
+  float s = 0.0f, c = 0.0f;  // chunks whose errors lie in [2^-40, 2^40]
+  double d = 0.0;            // other chunks (sums that fp32 would over- or underflow)
   float max_abs = 0.0f;
   float rel = 0.0f;   // this lane's exact best ratio
   float T = 0.0f;     // warp-uniform: max of `rel` over the warp
@@ -330,18 +333,30 @@ __device__ __forceinline__ float warp_max(float v);
 // data pass x = x^ = 0.
 template <int N>
 __device__ __forceinline__ void acc_chunk(StatAcc& acc, const float (&xs)[N], const float (&xh)[N]) {
-  float part = 0.0f;
   bool cand = false;
   const bool want_rel = acc.T < 1.0f;  // warp-uniform
   float e[N];
+  float cm = 0.0f;  // largest |e| of the chunk
 #pragma unroll
   for (int i = 0; i < N; ++i) {
     e[i] = __fsub_rn(xs[i], xh[i]);
-    part = __fmaf_rn(e[i], e[i], part);
-    acc.max_abs = fmaxf(acc.max_abs, fabsf(e[i]));
+    cm = fmaxf(cm, fabsf(e[i]));
     if (want_rel) cand |= rel_candidate(acc.T, xs[i], fabsf(e[i]));
   }
-  acc_add_sum(acc, part);
+  acc.max_abs = fmaxf(acc.max_abs, cm);
+  if (cm <= 0x1p40f && (cm >= 0x1p-40f || cm == 0.0f)) {
+    // every e^2 <= 2^80 and the chunk sum >= 2^-80: no overflow, and the squares that
+    // underflow (|e| < 2^-75) are below 2^-70 of the chunk's largest
+    float part = 0.0f;
+#pragma unroll
+    for (int i = 0; i < N; ++i) part = __fmaf_rn(e[i], e[i], part);
+    acc_add_sum(acc, part);
+  } else {
+    double part = 0.0;
+#pragma unroll
+    for (int i = 0; i < N; ++i) part = fma(static_cast<double>(e[i]), static_cast<double>(e[i]), part);
+    acc.d += part;
+  }
   if (want_rel && __any_sync(kFull, cand)) {
     if (cand) {
 #pragma unroll
@@ -369,7 +384,7 @@ __device__ __forceinline__ void stats_finish(const StatAcc& a, void* ws, qz_stat
   __shared__ float s_abs[kWarps], s_rel[kWarps];
   __shared__ bool s_last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  double sum = warp_sum(static_cast<double>(a.s) + static_cast<double>(a.c));
+  double sum = warp_sum(static_cast<double>(a.s) + static_cast<double>(a.c) + a.d);
   float mabs = warp_max(a.max_abs), mrel = warp_max(a.rel);
   if (lane == 0) {
     s_sum[warp] = sum;
