@@ -92,6 +92,8 @@ def assert_stats_close(s, o, what="stats"):
         assert getattr(s, f) == getattr(o, f), (what, f, getattr(s, f), getattr(o, f))
     for f in ("sum_sq_err", "mse"):
         a, b = getattr(s, f), getattr(o, f)
+        if a == b:  # includes equal infinities (x^ past the fp32 range, see below)
+            continue
         assert abs(a - b) <= STATS_RTOL * abs(b) + 1e-300, (what, f, a, b)
 
 
