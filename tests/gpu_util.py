@@ -92,7 +92,7 @@ def assert_stats_close(s, o, what="stats"):
         assert getattr(s, f) == getattr(o, f), (what, f, getattr(s, f), getattr(o, f))
     for f in ("sum_sq_err", "mse"):
         a, b = getattr(s, f), getattr(o, f)
-        if a == b:  # includes equal infinities (x^ past the fp32 range, see below)
+        if a == b:  # includes equal infinities (x^ past the binary32 range)
             continue
         assert abs(a - b) <= STATS_RTOL * abs(b) + 1e-300, (what, f, a, b)
 
