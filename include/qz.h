@@ -109,6 +109,8 @@ typedef enum { QZ_SCALE_UP = 0, QZ_SCALE_NEAREST = 1 } qz_scale_round;
 /* Status-word bits (qz_get_device_status). */
 #define QZ_FLAG_NONFINITE_INPUT 0x1u /* a NaN or Inf element was read                   */
 #define QZ_FLAG_BAD_AMAX 0x2u        /* a caller-supplied tensor amax was < 0 or NaN     */
+#define QZ_FLAG_PIPELINE_TIMEOUT 0x4u /* a kernel gave up waiting for its own staged copy   */
+                                      /* (never expected; re-initialise the workspace)   */
 
 typedef struct {
   int32_t format;      /* qz_format                                                  */

@@ -28,7 +28,7 @@ QZ_BF16, QZ_F32 = 1, 2
 QZ_GRAN_TENSOR, QZ_GRAN_ROW, QZ_GRAN_BLOCK, QZ_GRAN_UNIT = 1, 2, 3, 4
 QZ_ROUND_RNE = 0
 QZ_SCALE_UP, QZ_SCALE_NEAREST = 0, 1
-QZ_FLAG_NONFINITE_INPUT, QZ_FLAG_BAD_AMAX = 0x1, 0x2
+QZ_FLAG_NONFINITE_INPUT, QZ_FLAG_BAD_AMAX, QZ_FLAG_PIPELINE_TIMEOUT = 0x1, 0x2, 0x4
 
 FORMATS = {"int8": QZ_INT8, "e4m3": QZ_FP8_E4M3, "e5m2": QZ_FP8_E5M2,
            "mxfp4": QZ_MXFP4, "nvfp4": QZ_NVFP4}

@@ -1,0 +1,214 @@
+// qz_pipe.cuh -- shared-memory staging with 1-D bulk copies (cp.async.bulk + mbarrier) and
+// packed fp32 arithmetic (f32x2) for the streaming kernels of libqz (sm_103a).
+#pragma once
+
+#include <cstdint>
+
+#include "qz_device.cuh"
+
+namespace qz {
+
+// ---------------------------------------------------------------------------------------
+// packed fp32 pairs: one 64-bit register holds {lo, hi}; one instruction does both lanes
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t pk(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fma2_rm(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rm.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// fl32(x / s) for both lanes from r = RN(1/s) and ns = -s (the FMA-corrected quotient of
+// div_by).  The remainder fma rounds toward -inf: it is exact whenever the quotient
+// matters, and for x = +-0 it makes the remainder -0, so the final fma keeps the sign of
+// zero of x (-0 / s = -0) without a separate copysign.
+__device__ __forceinline__ uint64_t div2(uint64_t x, uint64_t r2, uint64_t ns2) {
+  const uint64_t q = mul2(x, r2);
+  const uint64_t rem = fma2_rm(q, ns2, x);
+  return fma2(rem, r2, q);
+}
+
+// largest magnitude of three with NaN propagation
+__device__ __forceinline__ float absmax3(float m, float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(m), "f"(fabsf(a)), "f"(fabsf(b)));
+  return d;
+}
+__device__ __forceinline__ float max3(float m, float a, float b) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(m), "f"(a), "f"(b));
+  return d;
+}
+
+// two bf16 in one word -> fp32 pair {lo, hi}
+__device__ __forceinline__ uint64_t widen_bf16x2(uint32_t w) {
+  return pk(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// Eight quotients -> one 32-bit word of E2M1 codes (element 0 in bits [0,4)) and the
+// decoded code values as four f16x2 words.
+__device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8], uint32_t (&h)[4]) {
+  uint32_t w;
+  asm("{\n\t.reg .b8 c0, c1, c2, c3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c0, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c1, %8, %7;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c2, %10, %9;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c3, %12, %11;\n\t"
+      "mov.b32 %0, {c0, c1, c2, c3};\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, c0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, c1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, c2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %4, c3;\n\t}"
+      : "=r"(w), "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return w;
+}
+// the same without the decoded values
+__device__ __forceinline__ uint32_t e2m1x8_codes(const float (&v)[8]) {
+  uint32_t w;
+  asm("{\n\t.reg .b8 c0, c1, c2, c3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c3, %8, %7;\n\t"
+      "mov.b32 %0, {c0, c1, c2, c3};\n\t}"
+      : "=r"(w)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return w;
+}
+// f16x2 -> fp32 pair (exact)
+__device__ __forceinline__ uint64_t f16x2_to_f32x2(uint32_t h) {
+  uint64_t r;
+  asm("{\n\t.reg .b16 l, h;\n\t.reg .f32 fl, fh;\n\tmov.b32 {l, h}, %1;\n\t"
+      "cvt.f32.f16 fl, l;\n\tcvt.f32.f16 fh, h;\n\tmov.b64 %0, {fl, fh};\n\t}"
+      : "=l"(r)
+      : "r"(h));
+  return r;
+}
+
+// ---------------------------------------------------------------------------------------
+// mbarrier + bulk copy global -> shared
+// ---------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Wait for phase `parity` of the barrier, giving up after `limit_ns` (returns false).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  return true;
+}
+// bytes (multiple of 16, both addresses 16-byte aligned) from global to shared; completion
+// is signalled on the barrier as transaction bytes
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void lds32B(uint32_t (&w)[8], uint32_t addr) {
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+               : "r"(addr));
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+               : "r"(addr + 16));
+}
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any copy's latency
+
+// Streams the tiles of one CTA through S shared-memory stages.  Tile k of this CTA is
+// tile (blockIdx.x + k * gridDim.x) of the tensor, TILE bytes (the last one shorter).
+// Thread 0 issues the copies; every thread waits on the tile's barrier.
+template <int S, int TILE>
+struct BulkPipe {
+  uint32_t base;      // shared address of stage 0
+  uint32_t bars;      // shared address of barrier 0
+  const char* src;
+  int64_t nbytes;
+  int64_t ntiles;
+
+  __device__ __forceinline__ int64_t tile_of(int64_t k) const {
+    return static_cast<int64_t>(blockIdx.x) + k * gridDim.x;
+  }
+  __device__ __forceinline__ uint32_t bytes_of(int64_t tile) const {
+    const int64_t rest = nbytes - tile * TILE;
+    return static_cast<uint32_t>(rest < TILE ? rest : TILE);
+  }
+  __device__ __forceinline__ void issue(int64_t k) const {  // thread 0 only
+    const int64_t tile = tile_of(k);
+    if (tile >= ntiles) return;
+    const uint32_t s = static_cast<uint32_t>(k % S);
+    const uint32_t bar = bars + 8u * s, bytes = bytes_of(tile);
+    mbar_expect_tx(bar, bytes);
+    bulk_g2s(base + s * TILE, src + tile * TILE, bytes, bar);
+  }
+  // thread 0, before the first tile (after the barriers are initialised and fenced)
+  __device__ __forceinline__ void prologue() const {
+    for (int k = 0; k < S; ++k) issue(k);
+  }
+  __device__ __forceinline__ bool wait(int64_t k) const {
+    const uint32_t s = static_cast<uint32_t>(k % S);
+    return mbar_wait(bars + 8u * s, static_cast<uint32_t>((k / S) & 1), kWaitLimitNs);
+  }
+  __device__ __forceinline__ uint32_t stage(int64_t k) const {
+    return base + static_cast<uint32_t>(k % S) * TILE;
+  }
+  // After an aborted wait: let the copies already issued for tiles k .. k+S-1 land
+  // (bounded) before the CTA's shared memory is released.
+  __device__ __forceinline__ void drain(int64_t k) const {
+    for (int64_t j = k; j < k + S; ++j)
+      if (tile_of(j) < ntiles) mbar_wait(bars + 8u * static_cast<uint32_t>(j % S),
+                                         static_cast<uint32_t>((j / S) & 1), kWaitLimitNs);
+  }
+};
+
+}  // namespace qz

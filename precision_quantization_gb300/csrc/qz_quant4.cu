@@ -9,6 +9,7 @@
 // per lane (coalesced); the first lane of every block stores its scale byte.
 #include "qz_device.cuh"
 #include "qz_internal.h"
+#include "qz_pipe.cuh"
 
 namespace qz {
 namespace {
@@ -188,8 +189,250 @@ __global__ void __launch_bounds__(kThreads) quant4_kernel(Q4Args a) {
   if constexpr (STATS) stats_finish(acc, a.ws, a.stats, static_cast<uint64_t>(g.rows * g.cols));
 }
 
+// ---------------------------------------------------------------------------------------
+// Dense tensors (rows back to back, 16-byte aligned): the input is streamed through shared
+// memory by 1-D bulk copies, 16 KiB per tile, 4 tiles in flight per CTA, so the memory
+// latency is covered by the pipeline instead of by registers.  The element arithmetic is
+// done on fp32 pairs (f32x2), which halves the FMA-pipe instructions, and the integer /
+// compare work is kept to 3-input max, the casts and the per-block scale.
+// ---------------------------------------------------------------------------------------
+constexpr int kCPT = 2;                      // 32-byte chunks per thread per tile
+constexpr int kTileChunks = kThreads * kCPT;
+constexpr int kTileBytes = kTileChunks * 32;  // 16 KiB
+constexpr int kStages = 4;
+constexpr size_t kPipeSmem = static_cast<size_t>(kStages) * kTileBytes;
+
+template <int FMT, int DT, bool UNIT, bool STATS>
+__global__ void __launch_bounds__(kThreads, 3) quant4_pipe_kernel(Q4Args a) {
+  constexpr int EPC = Elem<DT>::kPer32B;
+  constexpr int BS = FMT == QZ_MXFP4 ? 32 : 16;
+  constexpr int L = BS / EPC;
+  constexpr int NP = EPC / 2;  // fp32 pairs per chunk
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bars[kStages];
+  __shared__ float2 tab[128];  // NVFP4: (s, RN(1/s)) for every E4M3 block code
+  __shared__ int s_abort;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int64_t n_chunks = a.g.n_chunks;
+
+  float sg = 1.0f, rg = 1.0f;
+  if constexpr (FMT == QZ_NVFP4) {
+    if constexpr (!UNIT) {
+      const float alpha = *a.amax;
+      if ((!(alpha >= 0.0f) || !is_finite_f(alpha)) && blockIdx.x == 0 && tid == 0)
+        flag_status(a.ws, QZ_FLAG_BAD_AMAX);
+      sg = __fdiv_rn(alpha, 2688.0f);  // global_amax / (6 * 448)
+      if (sg == 0.0f) sg = 1.0f;
+      rg = __frcp_rn(sg);
+    }
+    for (int c = tid; c < 128; c += kThreads) {
+      const float s = __fmul_rn(sg, dec_e4m3(static_cast<uint32_t>(c)));
+      tab[c] = make_float2(s, (s > 0.0f && fast_div_ok(s)) ? __frcp_rn(s) : 0.0f);
+    }
+  }
+  if (a.tscale_out && blockIdx.x == 0 && tid == 0) *a.tscale_out = sg;
+  if (tid == 0) {
+    for (int i = 0; i < kStages; ++i) mbar_init(smem_addr(&bars[i]), 1);
+    mbar_init_fence();
+    s_abort = 0;
+  }
+  __syncthreads();
+  BulkPipe<kStages, kTileBytes> P{smem_addr(smem), smem_addr(&bars[0]),
+                                  static_cast<const char*>(a.x), n_chunks * 32,
+                                  (n_chunks + kTileChunks - 1) / kTileChunks};
+  if (tid == 0) P.prologue();
+
+  StatAcc acc;
+  for (int64_t k = 0; P.tile_of(k) < P.ntiles; ++k) {
+    const int64_t tile = P.tile_of(k);
+    if (!P.wait(k)) s_abort = 1;
+    const uint32_t stage = P.stage(k);
+#pragma unroll
+    for (int c = 0; c < kCPT; ++c) {
+      const int j = c * kThreads + tid;
+      const int64_t u = tile * kTileChunks + j;  // global 32-byte chunk
+      const bool valid = u < n_chunks;
+      uint32_t w[8];
+      if (valid) {
+        lds32B(w, stage + 32u * j);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = 0u;
+      }
+      // widen to fp32 pairs; block amax (NaN propagates)
+      uint64_t xp[NP];
+      float A = 0.0f;
+#pragma unroll
+      for (int p = 0; p < NP; ++p) {
+        float lo, hi;
+        if constexpr (DT == QZ_BF16) {
+          lo = __uint_as_float(w[p] << 16);
+          hi = __uint_as_float(w[p] & 0xffff0000u);
+        } else {
+          lo = __uint_as_float(w[2 * p]);
+          hi = __uint_as_float(w[2 * p + 1]);
+        }
+        xp[p] = pk(lo, hi);
+        A = absmax3(A, lo, hi);
+      }
+      if constexpr (L >= 2) A = absmax_nan(A, __shfl_xor_sync(kFull, A, 1));
+      if constexpr (L >= 4) A = absmax_nan(A, __shfl_xor_sync(kFull, A, 2));
+      if (valid && !is_finite_f(A)) flag_status(a.ws, QZ_FLAG_NONFINITE_INPUT);
+
+      // block scale s and the quotients v = fl32(x / s), as fp32 pairs
+      uint32_t scode;
+      float s;
+      uint64_t vp[NP];
+      bool mul_exact = false;  // MXFP4: decode(q) * s exact, e = fma(-q, s, x)
+      if constexpr (FMT == QZ_MXFP4) {
+        const int kexp = UNIT ? 0 : mx_exponent(div6(A), a.scale_round);
+        scode = static_cast<uint32_t>(kexp + 127);
+        s = exp2_pos(kexp);
+        const float inv = exp2_neg(kexp);
+        const uint64_t inv2 = pk(inv, inv);
+#pragma unroll
+        for (int p = 0; p < NP; ++p) vp[p] = mul2(xp[p], inv2);
+        mul_exact = kexp >= -125 && kexp <= 125;
+      } else {
+        if constexpr (UNIT) {
+          scode = 0x38u;
+        } else {
+          scode = nv_block_code(div_scalar(div6(A), sg, rg), a.scale_round);
+        }
+        const float2 sr = tab[scode];
+        s = sr.x;
+        if (sr.y != 0.0f && __fmul_rn(A, sr.y) <= 0x1p100f) {
+          const uint64_t r2 = pk(sr.y, sr.y), ns2 = pk(-s, -s);
+#pragma unroll
+          for (int p = 0; p < NP; ++p) vp[p] = div2(xp[p], r2, ns2);
+        } else if (s == 0.0f) {
+          const uint64_t z2 = pk(0.0f, 0.0f);
+#pragma unroll
+          for (int p = 0; p < NP; ++p) vp[p] = mul2(xp[p], z2);  // signed zeros
+        } else {
+#pragma unroll
+          for (int p = 0; p < NP; ++p) {
+            float lo, hi;
+            upk(xp[p], lo, hi);
+            vp[p] = pk(__fdiv_rn(lo, s), __fdiv_rn(hi, s));
+          }
+        }
+      }
+
+      // cast and pack 8 at a time; store the codes and the block scale
+      uint32_t cw[EPC / 8];
+      uint32_t h[EPC / 8][4];
+#pragma unroll
+      for (int g8 = 0; g8 < EPC / 8; ++g8) {
+        float v[8];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) upk(vp[4 * g8 + p], v[2 * p], v[2 * p + 1]);
+        if constexpr (STATS) cw[g8] = e2m1x8(v, h[g8]);
+        else cw[g8] = e2m1x8_codes(v);
+      }
+      if (valid) {
+        uint8_t* cp = a.codes + u * (EPC / 2);
+        if constexpr (EPC == 16) {
+          asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(cp), "r"(cw[0]), "r"(cw[1]) : "memory");
+        } else {
+          asm volatile("st.global.u32 [%0], %1;" ::"l"(cp), "r"(cw[0]) : "memory");
+        }
+        if (lane % L == 0) a.scales[u / L] = static_cast<uint8_t>(scode);
+      }
+
+      if constexpr (STATS) {
+        // x^ = fl32(decode(q) * s), e = fl32(x - x^); lanes without data hold x = 0, q = 0
+        const uint64_t s2 = pk(s, s), ns2 = pk(-s, -s);
+        uint64_t e2[NP];
+        uint64_t part2 = pk(0.0f, 0.0f);
+        float cm = 0.0f;
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+          const uint64_t q2 = f16x2_to_f32x2(h[p / 4][p % 4]);
+          e2[p] = mul_exact ? fma2(q2, ns2, xp[p]) : sub2(xp[p], mul2(q2, s2));
+          part2 = fma2(e2[p], e2[p], part2);
+          float e0, e1;
+          upk(e2[p], e0, e1);
+          cm = max3(cm, fabsf(e0), fabsf(e1));
+        }
+        acc.max_abs = fmaxf(acc.max_abs, cm);
+        if (cm <= 0x1p40f && (cm >= 0x1p-40f || cm == 0.0f)) {
+          float p0, p1;
+          upk(part2, p0, p1);
+          acc_add_sum(acc, __fadd_rn(p0, p1));
+        } else {
+          double d = 0.0;
+#pragma unroll
+          for (int p = 0; p < NP; ++p) {
+            float e0, e1;
+            upk(e2[p], e0, e1);
+            d = fma(static_cast<double>(e0), static_cast<double>(e0), d);
+            d = fma(static_cast<double>(e1), static_cast<double>(e1), d);
+          }
+          acc.d += d;
+        }
+        if (acc.T < 1.0f) {  // warp-uniform; see rel_candidate
+          bool cand = false;
+#pragma unroll
+          for (int p = 0; p < NP; ++p) {
+            float x0, x1, e0, e1;
+            upk(xp[p], x0, x1);
+            upk(e2[p], e0, e1);
+            cand |= rel_candidate(acc.T, x0, fabsf(e0)) | rel_candidate(acc.T, x1, fabsf(e1));
+          }
+          if (__any_sync(kFull, cand)) {
+            if (cand) {
+#pragma unroll
+              for (int p = 0; p < NP; ++p) {
+                float x0, x1, e0, e1;
+                upk(xp[p], x0, x1);
+                upk(e2[p], e0, e1);
+                acc.rel = max3(acc.rel, rel_exact(x0, fabsf(e0)), rel_exact(x1, fabsf(e1)));
+              }
+            }
+            acc.T = warp_max(acc.rel);
+          }
+        }
+      }
+    }
+    __syncthreads();  // every thread is done with this stage
+    if (s_abort) {
+      if (tid == 0) {
+        flag_status(a.ws, QZ_FLAG_PIPELINE_TIMEOUT);
+        P.drain(k);
+      }
+      return;
+    }
+    if (tid == 0) P.issue(k + kStages);
+  }
+  if constexpr (STATS) stats_finish(acc, a.ws, a.stats, static_cast<uint64_t>(a.g.rows * a.g.cols));
+}
+
+template <int FMT, int DT, bool UNIT, bool STATS>
+qz_status run_pipe(const Q4Args& args, cudaStream_t s) {
+  auto kern = &quant4_pipe_kernel<FMT, DT, UNIT, STATS>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kPipeSmem)) != cudaSuccess)
+    return QZ_ERR_CUDA;
+  int dev = 0, sms = 1, occ = 1;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, kPipeSmem);
+  const int64_t tiles = (args.g.n_chunks + kTileChunks - 1) / kTileChunks;
+  int64_t grid = static_cast<int64_t>(sms) * (occ < 1 ? 1 : occ);
+  if (tiles < grid) grid = tiles;
+  if (grid < 1) grid = 1;
+  if (grid > kMaxCtas) grid = kMaxCtas;
+  kern<<<static_cast<int>(grid), kThreads, kPipeSmem, s>>>(args);
+  return launch_status();
+}
+
 template <int FMT, int DT, bool UNIT, bool STATS, bool VEC>
 qz_status run(const Q4Args& args, cudaStream_t s) {
+  if constexpr (VEC) {
+    if (args.g.dense && reinterpret_cast<uintptr_t>(args.x) % 16 == 0)
+      return run_pipe<FMT, DT, UNIT, STATS>(args, s);
+  }
   auto kern = &quant4_kernel<FMT, DT, UNIT, STATS, VEC>;
   const int64_t per_cta = static_cast<int64_t>(kThreads) * kUnroll;
   const int grid = grid_for(reinterpret_cast<const void*>(kern), (args.g.n_chunks + per_cta - 1) / per_cta, s);
