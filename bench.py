@@ -32,6 +32,7 @@ ROWS, COLS = 32768, 8192
 WORKLOAD = "lognormal-stream-32768x8192-bf16"
 L2_FLUSH_BYTES = 256 << 20
 KERNEL_SOURCES = ["precision_quantization_gb300/csrc/qz_device.cuh",
+                  "precision_quantization_gb300/csrc/qz_pipe.cuh",
                   "precision_quantization_gb300/csrc/qz_quant4.cu",
                   "precision_quantization_gb300/csrc/qz_dequant.cu",
                   "precision_quantization_gb300/csrc/qz_amax.cu"]

@@ -7,11 +7,54 @@
 // value, so a single comparison at the end detects non-finite input.
 #include "qz_device.cuh"
 #include "qz_internal.h"
+#include "qz_pipe.cuh"
 
 namespace qz {
 namespace {
 
 constexpr int kUnroll = 4;
+
+// CTA maximum of per-thread maxima (m: bf16 -> two 16-bit magnitudes, fp32 -> one), written
+// as this CTA's partial; the last CTA to finish folds the partials into *out and flags a
+// non-finite maximum.
+template <int DT>
+__device__ __forceinline__ void amax_finish(uint32_t m, float* out, void* ws) {
+  uint32_t bits;  // fp32 bit pattern of this thread's maximum
+  if constexpr (DT == QZ_BF16) bits = max(m & 0xffffu, m >> 16) << 16;
+  else bits = m;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) bits = max(bits, __shfl_xor_sync(kFull, bits, o));
+  __shared__ uint32_t s_w[kWarps];
+  __shared__ bool s_last;
+  if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = bits;
+  __syncthreads();
+  float* parts = ws_amax_partials(ws);
+  if (threadIdx.x == 0) {
+    uint32_t b = 0;
+    for (int w = 0; w < kWarps; ++w) b = max(b, s_w[w]);
+    reinterpret_cast<uint32_t*>(parts)[blockIdx.x] = b;
+    __threadfence();
+    const uint32_t done = atomicInc(&ws_header(ws)->amax_counter, gridDim.x - 1);
+    s_last = (done == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  uint32_t b = 0;
+  for (int i = threadIdx.x; i < static_cast<int>(gridDim.x); i += kThreads)
+    b = max(b, reinterpret_cast<volatile uint32_t*>(parts)[i]);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) b = max(b, __shfl_xor_sync(kFull, b, o));
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = b;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t t = 0;
+    for (int w = 0; w < kWarps; ++w) t = max(t, s_w[w]);
+    if (t >= 0x7f800000u) atomicOr(&ws_header(ws)->status, QZ_FLAG_NONFINITE_INPUT);
+    *out = __uint_as_float(t);
+  }
+}
 
 template <int DT, bool VEC>
 __global__ void __launch_bounds__(kThreads)
@@ -57,46 +100,72 @@ amax_kernel(const void* __restrict__ x, Geom g, float* __restrict__ out, void* w
       else m = max(m, b);
     }
   }
-  uint32_t bits;  // fp32 bit pattern of this thread's maximum
-  if constexpr (DT == QZ_BF16) bits = max(m & 0xffffu, m >> 16) << 16;
-  else bits = m;
-#pragma unroll
-  for (int o = 16; o; o >>= 1) bits = max(bits, __shfl_xor_sync(kFull, bits, o));
-  __shared__ uint32_t s_w[kWarps];
-  __shared__ bool s_last;
-  if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = bits;
-  __syncthreads();
-  float* parts = ws_amax_partials(ws);
-  if (threadIdx.x == 0) {
-    uint32_t b = 0;
-    for (int w = 0; w < kWarps; ++w) b = max(b, s_w[w]);
-    reinterpret_cast<uint32_t*>(parts)[blockIdx.x] = b;
-    __threadfence();
-    const uint32_t done = atomicInc(&ws_header(ws)->amax_counter, gridDim.x - 1);
-    s_last = (done == gridDim.x - 1);
+  amax_finish<DT>(m, out, ws);
+}
+
+// Dense tensors: x streamed through shared memory by 1-D bulk copies (16 KiB tiles, four
+// in flight per CTA), so the read runs at the copy engine's pace whatever the occupancy.
+template <int DT>
+__global__ void __launch_bounds__(kThreads)
+amax_pipe_kernel(const void* __restrict__ x, int64_t n_chunks, float* __restrict__ out, void* ws) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bars[kPipeStages];
+  __shared__ int s_abort;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    for (int i = 0; i < kPipeStages; ++i) mbar_init(smem_addr(&bars[i]), 1);
+    mbar_init_fence();
+    s_abort = 0;
   }
   __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  uint32_t b = 0;
-  for (int i = threadIdx.x; i < static_cast<int>(gridDim.x); i += kThreads)
-    b = max(b, reinterpret_cast<volatile uint32_t*>(parts)[i]);
+  BulkPipe<kPipeStages, kPipeTileBytes> P{smem_addr(smem), smem_addr(&bars[0]),
+                                          static_cast<const char*>(x), n_chunks * 32,
+                                          (n_chunks + kPipeTileChunks - 1) / kPipeTileChunks, false};
+  if (tid == 0) P.prologue();
+  uint32_t m = 0;
+  for (int64_t k = 0; P.has(k); ++k) {
+    const int64_t tile = P.tile_of(k);
+    if (!P.wait(k)) s_abort = 1;
+    const uint32_t stage = P.stage(k);
 #pragma unroll
-  for (int o = 16; o; o >>= 1) b = max(b, __shfl_xor_sync(kFull, b, o));
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = b;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    uint32_t t = 0;
-    for (int w = 0; w < kWarps; ++w) t = max(t, s_w[w]);
-    if (t >= 0x7f800000u) atomicOr(&ws_header(ws)->status, QZ_FLAG_NONFINITE_INPUT);
-    *out = __uint_as_float(t);
+    for (int c = 0; c < kPipeCPT; ++c) {
+      const int j = c * kThreads + tid;
+      if (tile * kPipeTileChunks + j < n_chunks) {
+        uint32_t w[8];
+        lds32B(w, stage + 32u * j);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if constexpr (DT == QZ_BF16) m = __vmaxu2(m, w[i] & 0x7fff7fffu);
+          else m = max(m, w[i] & 0x7fffffffu);
+        }
+      }
+    }
+    __syncthreads();
+    if (s_abort) {
+      if (tid == 0) {
+        flag_status(ws, QZ_FLAG_PIPELINE_TIMEOUT);
+        P.drain(k);
+      }
+      return;
+    }
+    if (tid == 0) P.issue(k + kPipeStages);
   }
+  amax_finish<DT>(m, out, ws);
 }
 
 template <int DT>
 qz_status run(const qz_desc& d, const void* x, float* out, void* ws, cudaStream_t s) {
   const Geom g = make_geom(d, x, Elem<DT>::kBytes, 32);
+  if (g.vec && g.dense) {
+    auto kern = &amax_pipe_kernel<DT>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kPipeSmem)) != cudaSuccess)
+      return QZ_ERR_CUDA;
+    const int grid = grid_for(reinterpret_cast<const void*>(kern),
+                              (g.n_chunks + kPipeTileChunks - 1) / kPipeTileChunks, s, kPipeSmem);
+    kern<<<grid, kThreads, kPipeSmem, s>>>(x, g.n_chunks, out, ws);
+    return launch_status();
+  }
   if (g.vec) {
     const void* k = reinterpret_cast<const void*>(&amax_kernel<DT, true>);
     const int grid = grid_for(k, (g.n_chunks + kThreads * kUnroll - 1) / (kThreads * kUnroll), s);

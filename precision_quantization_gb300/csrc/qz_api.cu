@@ -24,11 +24,11 @@ Geom make_geom(const qz_desc& d, const void* hp, int eb, int align) {
   return g;
 }
 
-int grid_for(const void* kernel, int64_t work_ctas, cudaStream_t) {
+int grid_for(const void* kernel, int64_t work_ctas, cudaStream_t, size_t dyn_smem) {
   int dev = 0, sms = 1, occ = 1;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, 0);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, dyn_smem);
   if (occ < 1) occ = 1;
   int64_t g = static_cast<int64_t>(sms) * occ;
   if (work_ctas < g) g = work_ctas;

@@ -11,6 +11,8 @@
 namespace qz {
 namespace {
 
+constexpr int kUnroll = 4;  // chunks per thread in flight
+
 struct DqArgs {
   const uint8_t* codes;
   const void* scales;
@@ -54,48 +56,61 @@ __global__ void __launch_bounds__(kThreads) dequant4_kernel(DqArgs a) {
   const uint8_t* sc = static_cast<const uint8_t*>(a.scales);
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
   const int64_t nthr = static_cast<int64_t>(gridDim.x) * kThreads;
-  for (int64_t u = tid; u < g.n_chunks; u += nthr) {
-    int64_t row, col;
-    if (g.dense) {
-      row = 0;
-      col = u * EPC;
-    } else {
-      row = u / g.cpr;
-      col = (u - row * g.cpr) * EPC;
-    }
-    const int64_t cofs = g.dense ? col / 2 : row * (g.cols / 2) + col / 2;
-    const int64_t sofs = g.dense ? col / BS : row * (g.cols / BS) + col / BS;
-    uint32_t cw[2];
-    if constexpr (VEC) {
-      if constexpr (CB == 8) {
-        const uint2 v = ld8B(a.codes + cofs);
-        cw[0] = v.x;
-        cw[1] = v.y;
+  for (int64_t base = tid; base < g.n_chunks; base += nthr * kUnroll) {
+    // all loads of the kUnroll chunks first, then the arithmetic and the stores
+    uint32_t cw[kUnroll][2];
+    uint32_t sc_code[kUnroll];
+    int64_t row[kUnroll], col[kUnroll];
+#pragma unroll
+    for (int k = 0; k < kUnroll; ++k) {
+      const int64_t u = base + k * nthr;
+      if (g.dense) {
+        row[k] = 0;
+        col[k] = u * EPC;
       } else {
-        cw[0] = ld4B(a.codes + cofs);
-        cw[1] = 0;
+        row[k] = u / g.cpr;
+        col[k] = (u - row[k] * g.cpr) * EPC;
       }
-    } else {
-      cw[0] = cw[1] = 0;
+      cw[k][0] = cw[k][1] = 0u;
+      sc_code[k] = 127u;
+      if (u < g.n_chunks) {
+        const int64_t cofs = g.dense ? col[k] / 2 : row[k] * (g.cols / 2) + col[k] / 2;
+        const int64_t sofs = g.dense ? col[k] / BS : row[k] * (g.cols / BS) + col[k] / BS;
+        if constexpr (VEC) {
+          if constexpr (CB == 8) {
+            const uint2 v = ld8B(a.codes + cofs);
+            cw[k][0] = v.x;
+            cw[k][1] = v.y;
+          } else {
+            cw[k][0] = ld4B(a.codes + cofs);
+          }
+        } else {
 #pragma unroll
-      for (int j = 0; j < CB; ++j) cw[j / 4] |= static_cast<uint32_t>(a.codes[cofs + j]) << (8 * (j % 4));
+          for (int j = 0; j < CB; ++j) cw[k][j / 4] |= static_cast<uint32_t>(a.codes[cofs + j]) << (8 * (j % 4));
+        }
+        if constexpr (!UNIT) sc_code[k] = ld1B(sc + sofs);
+      }
     }
-    float s;
-    if constexpr (FMT == QZ_MXFP4) {
-      const uint32_t c = UNIT ? 127u : ld1B(sc + sofs);
-      s = c == 255u ? __uint_as_float(0x7fc00000u) : exp2_pos(static_cast<int>(c) - 127);
-    } else {
-      s = UNIT ? 1.0f : __fmul_rn(sg, dec_e4m3(ld1B(sc + sofs)));
-    }
-    float xh[EPC];
 #pragma unroll
-    for (int j = 0; j < CB; ++j) {
-      float q0, q1;
-      dec_e2m1x2((cw[j / 4] >> (8 * (j % 4))) & 0xffu, q0, q1);
-      xh[2 * j] = __fmul_rn(q0, s);
-      xh[2 * j + 1] = __fmul_rn(q1, s);
+    for (int k = 0; k < kUnroll; ++k) {
+      if (base + k * nthr >= g.n_chunks) break;
+      float s;
+      if constexpr (FMT == QZ_MXFP4) {
+        const uint32_t c = UNIT ? 127u : sc_code[k];
+        s = c == 255u ? __uint_as_float(0x7fc00000u) : exp2_pos(static_cast<int>(c) - 127);
+      } else {
+        s = UNIT ? 1.0f : __fmul_rn(sg, dec_e4m3(sc_code[k]));
+      }
+      float xh[EPC];
+#pragma unroll
+      for (int j = 0; j < CB; ++j) {
+        float q0, q1;
+        dec_e2m1x2((cw[k][j / 4] >> (8 * (j % 4))) & 0xffu, q0, q1);
+        xh[2 * j] = __fmul_rn(q0, s);
+        xh[2 * j + 1] = __fmul_rn(q1, s);
+      }
+      put_chunk<ODT>(a.y, g, row[k], col[k], EPC, xh, VEC);
     }
-    put_chunk<ODT>(a.y, g, row, col, EPC, xh, VEC);
   }
 }
 
@@ -108,57 +123,70 @@ __global__ void __launch_bounds__(kThreads) dequant8_kernel(DqArgs a) {
   if constexpr (GRAN == QZ_GRAN_TENSOR) st = *a.tscale;
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
   const int64_t nthr = static_cast<int64_t>(gridDim.x) * kThreads;
-  for (int64_t u = tid; u < g.n_chunks; u += nthr) {
-    int64_t row, col;
-    if (g.dense) {
-      row = 0;
-      col = u * EPC;
-    } else {
-      row = u / g.cpr;
-      col = (u - row * g.cpr) * EPC;
-    }
-    const int64_t nv = g.dense ? EPC : g.cols - col;
-    const uint8_t* cp = a.codes + (g.dense ? col : row * g.cols + col);
-    uint32_t cw[EPC / 4];
-    if constexpr (VEC) {
-      if constexpr (EPC == 16) {
-        const uint4 v = ld16B(cp);
-        cw[0] = v.x;
-        cw[1] = v.y;
-        cw[2] = v.z;
-        cw[3] = v.w;
+  for (int64_t base = tid; base < g.n_chunks; base += nthr * kUnroll) {
+    uint32_t cw[kUnroll][EPC / 4];
+    float sk[kUnroll];
+    int64_t row[kUnroll], col[kUnroll];
+#pragma unroll
+    for (int k = 0; k < kUnroll; ++k) {
+      const int64_t u = base + k * nthr;
+      if (g.dense) {
+        row[k] = 0;
+        col[k] = u * EPC;
       } else {
-        const uint2 v = ld8B(cp);
-        cw[0] = v.x;
-        cw[1] = v.y;
+        row[k] = u / g.cpr;
+        col[k] = (u - row[k] * g.cpr) * EPC;
       }
-    } else {
 #pragma unroll
-      for (int j = 0; j < EPC / 4; ++j) cw[j] = 0;
+      for (int j = 0; j < EPC / 4; ++j) cw[k][j] = 0u;
+      sk[k] = st;
+      if (u < g.n_chunks) {
+        const int64_t nv = g.dense ? EPC : g.cols - col[k];
+        const uint8_t* cp = a.codes + (g.dense ? col[k] : row[k] * g.cols + col[k]);
+        if constexpr (VEC) {
+          if constexpr (EPC == 16) {
+            const uint4 v = ld16B(cp);
+            cw[k][0] = v.x;
+            cw[k][1] = v.y;
+            cw[k][2] = v.z;
+            cw[k][3] = v.w;
+          } else {
+            const uint2 v = ld8B(cp);
+            cw[k][0] = v.x;
+            cw[k][1] = v.y;
+          }
+        } else {
 #pragma unroll
-      for (int j = 0; j < EPC; ++j)
-        if (j < nv) cw[j / 4] |= static_cast<uint32_t>(cp[j]) << (8 * (j % 4));
+          for (int j = 0; j < EPC; ++j)
+            if (j < nv) cw[k][j / 4] |= static_cast<uint32_t>(cp[j]) << (8 * (j % 4));
+        }
+        if constexpr (GRAN == QZ_GRAN_ROW) {
+          const int64_t r = g.dense ? (col[k] / g.cols) : row[k];
+          sk[k] = static_cast<const float*>(a.scales)[r];
+        }
+      }
     }
-    float s = st;
-    if constexpr (GRAN == QZ_GRAN_ROW) {
-      const int64_t r = g.dense ? (col / g.cols) : row;
-      s = static_cast<const float*>(a.scales)[r];
-    }
-    float xh[EPC];
 #pragma unroll
-    for (int j = 0; j < EPC / 2; ++j) {
-      float q0, q1;
-      dec8x2<FMT>((cw[j / 2] >> (16 * (j % 2))) & 0xffffu, q0, q1);
-      xh[2 * j] = __fmul_rn(q0, s);
-      xh[2 * j + 1] = __fmul_rn(q1, s);
+    for (int k = 0; k < kUnroll; ++k) {
+      const int64_t u = base + k * nthr;
+      if (u >= g.n_chunks) break;
+      const int64_t nv = g.dense ? EPC : g.cols - col[k];
+      float xh[EPC];
+#pragma unroll
+      for (int j = 0; j < EPC / 2; ++j) {
+        float q0, q1;
+        dec8x2<FMT>((cw[k][j / 2] >> (16 * (j % 2))) & 0xffffu, q0, q1);
+        xh[2 * j] = __fmul_rn(q0, sk[k]);
+        xh[2 * j + 1] = __fmul_rn(q1, sk[k]);
+      }
+      put_chunk<ODT>(a.y, g, row[k], col[k], nv, xh, VEC);
     }
-    put_chunk<ODT>(a.y, g, row, col, nv, xh, VEC);
   }
 }
 
 template <typename K>
 qz_status go(K kern, const DqArgs& args, cudaStream_t s) {
-  const int64_t work = (args.g.n_chunks + kThreads - 1) / kThreads;
+  const int64_t work = (args.g.n_chunks + kThreads * kUnroll - 1) / (kThreads * kUnroll);
   const int grid = grid_for(reinterpret_cast<const void*>(kern), work, s);
   kern<<<grid, kThreads, 0, s>>>(args);
   return launch_status();

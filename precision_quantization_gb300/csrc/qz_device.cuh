@@ -250,9 +250,15 @@ struct Fmt8 {
 // ---------------------------------------------------------------------------------------
 constexpr float kRcp6 = 0x1.555556p-3f;  // RN(1/6)
 
-// fl32(A / 6)
+// fl32(a / s) for a >= 0 (no sign of zero to keep), from r = RN(1/s)
+__device__ __forceinline__ float div_pos(float a, float s, float r) {
+  const float q = __fmul_rn(a, r);
+  return __fmaf_rn(__fmaf_rn(-q, s, a), r, q);
+}
+
+// fl32(A / 6), A >= 0
 __device__ __forceinline__ float div6(float A) {
-  return A >= 0x1p-100f ? div_by(A, 6.0f, kRcp6) : __fdiv_rn(A, 6.0f);
+  return A >= 0x1p-100f ? div_pos(A, 6.0f, kRcp6) : __fdiv_rn(A, 6.0f);
 }
 
 // MXFP4: exponent k of the E8M0 scale 2^k from t = fl32(A/6); UP: smallest k with

@@ -22,7 +22,7 @@ Geom make_geom(const qz_desc& d, const void* hp, int elem_bytes, int align_bytes
 
 // Persistent-grid size: resident CTAs of `kernel` on every SM, capped by the work and by
 // the partial-result slots of the workspace.
-int grid_for(const void* kernel, int64_t work_ctas, cudaStream_t stream);
+int grid_for(const void* kernel, int64_t work_ctas, cudaStream_t stream, size_t dyn_smem = 0);
 
 qz_status launch_amax(const qz_desc& d, const void* x, float* out, void* ws, cudaStream_t s);
 

@@ -40,6 +40,15 @@ __device__ __forceinline__ uint64_t fma2_rm(uint64_t a, uint64_t b, uint64_t c) 
   return d;
 }
 
+// fl32(a * b) for both lanes as an fma with a -0 addend.  A separate mul.rn.f32x2 whose
+// result feeds a sub.rn.f32x2 can be contracted into one fma by the assembler, which skips
+// the rounding of the product; an fma cannot be merged further.
+__device__ __forceinline__ uint64_t mul2_rounded(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(0x8000000080000000ull));
+  return d;
+}
+
 // fl32(x / s) for both lanes from r = RN(1/s) and ns = -s (the FMA-corrected quotient of
 // div_by).  The remainder fma rounds toward -inf: it is exact whenever the quotient
 // matters, and for x = +-0 it makes the remainder -0, so the final fma keeps the sign of
@@ -165,8 +174,17 @@ __device__ __forceinline__ void lds32B(uint32_t (&w)[8], uint32_t addr) {
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any copy's latency
 
+// Geometry of the staged streaming kernels: a tile is kPipeCPT 32-byte chunks per thread
+// (16 KiB for 256 threads), kPipeStages tiles in flight per CTA.
+constexpr int kPipeCPT = 2;
+constexpr int kPipeTileChunks = kThreads * kPipeCPT;
+constexpr int kPipeTileBytes = kPipeTileChunks * 32;
+constexpr int kPipeStages = 4;
+constexpr size_t kPipeSmem = static_cast<size_t>(kPipeStages) * kPipeTileBytes;
+
 // Streams the tiles of one CTA through S shared-memory stages.  Tile k of this CTA is
-// tile (blockIdx.x + k * gridDim.x) of the tensor, TILE bytes (the last one shorter).
+// tile (blockIdx.x + k * gridDim.x) of the tensor (counted from the end when `reverse`),
+// TILE bytes (the last tile of the tensor shorter).
 // Thread 0 issues the copies; every thread waits on the tile's barrier.
 template <int S, int TILE>
 struct BulkPipe {
@@ -175,17 +193,23 @@ struct BulkPipe {
   const char* src;
   int64_t nbytes;
   int64_t ntiles;
+  bool reverse;  // hand out the tiles from the end of the tensor
 
-  __device__ __forceinline__ int64_t tile_of(int64_t k) const {
+  __device__ __forceinline__ int64_t slot_of(int64_t k) const {
     return static_cast<int64_t>(blockIdx.x) + k * gridDim.x;
+  }
+  __device__ __forceinline__ bool has(int64_t k) const { return slot_of(k) < ntiles; }
+  __device__ __forceinline__ int64_t tile_of(int64_t k) const {
+    const int64_t t = slot_of(k);
+    return reverse ? ntiles - 1 - t : t;
   }
   __device__ __forceinline__ uint32_t bytes_of(int64_t tile) const {
     const int64_t rest = nbytes - tile * TILE;
     return static_cast<uint32_t>(rest < TILE ? rest : TILE);
   }
   __device__ __forceinline__ void issue(int64_t k) const {  // thread 0 only
+    if (!has(k)) return;
     const int64_t tile = tile_of(k);
-    if (tile >= ntiles) return;
     const uint32_t s = static_cast<uint32_t>(k % S);
     const uint32_t bar = bars + 8u * s, bytes = bytes_of(tile);
     mbar_expect_tx(bar, bytes);
@@ -206,7 +230,7 @@ struct BulkPipe {
   // (bounded) before the CTA's shared memory is released.
   __device__ __forceinline__ void drain(int64_t k) const {
     for (int64_t j = k; j < k + S; ++j)
-      if (tile_of(j) < ntiles) mbar_wait(bars + 8u * static_cast<uint32_t>(j % S),
+      if (has(j)) mbar_wait(bars + 8u * static_cast<uint32_t>(j % S),
                                          static_cast<uint32_t>((j / S) & 1), kWaitLimitNs);
   }
 };

@@ -26,6 +26,7 @@ struct Q4Args {
   qz_stats* stats;
   void* ws;
   int scale_round;
+  bool reverse;  // pipelined path: walk the tiles from the end of the tensor
 };
 
 // fl32(a / b) for scalar scale arithmetic: the FMA-corrected quotient where it is exact
@@ -196,13 +197,12 @@ __global__ void __launch_bounds__(kThreads) quant4_kernel(Q4Args a) {
 // done on fp32 pairs (f32x2), which halves the FMA-pipe instructions, and the integer /
 // compare work is kept to 3-input max, the casts and the per-block scale.
 // ---------------------------------------------------------------------------------------
-constexpr int kCPT = 2;                      // 32-byte chunks per thread per tile
-constexpr int kTileChunks = kThreads * kCPT;
-constexpr int kTileBytes = kTileChunks * 32;  // 16 KiB
-constexpr int kStages = 4;
-constexpr size_t kPipeSmem = static_cast<size_t>(kStages) * kTileBytes;
+constexpr int kCPT = kPipeCPT;
+constexpr int kTileChunks = kPipeTileChunks;
+constexpr int kTileBytes = kPipeTileBytes;
+constexpr int kStages = kPipeStages;
 
-template <int FMT, int DT, bool UNIT, bool STATS>
+template <int FMT, int DT, bool UNIT, bool STATS, int SR>
 __global__ void __launch_bounds__(kThreads, 3) quant4_pipe_kernel(Q4Args a) {
   constexpr int EPC = Elem<DT>::kPer32B;
   constexpr int BS = FMT == QZ_MXFP4 ? 32 : 16;
@@ -216,6 +216,7 @@ __global__ void __launch_bounds__(kThreads, 3) quant4_pipe_kernel(Q4Args a) {
   const int64_t n_chunks = a.g.n_chunks;
 
   float sg = 1.0f, rg = 1.0f;
+  bool sg_fast = true;
   if constexpr (FMT == QZ_NVFP4) {
     if constexpr (!UNIT) {
       const float alpha = *a.amax;
@@ -225,6 +226,7 @@ __global__ void __launch_bounds__(kThreads, 3) quant4_pipe_kernel(Q4Args a) {
       if (sg == 0.0f) sg = 1.0f;
       rg = __frcp_rn(sg);
     }
+    sg_fast = fast_div_ok(sg);
     for (int c = tid; c < 128; c += kThreads) {
       const float s = __fmul_rn(sg, dec_e4m3(static_cast<uint32_t>(c)));
       tab[c] = make_float2(s, (s > 0.0f && fast_div_ok(s)) ? __frcp_rn(s) : 0.0f);
@@ -239,13 +241,14 @@ __global__ void __launch_bounds__(kThreads, 3) quant4_pipe_kernel(Q4Args a) {
   __syncthreads();
   BulkPipe<kStages, kTileBytes> P{smem_addr(smem), smem_addr(&bars[0]),
                                   static_cast<const char*>(a.x), n_chunks * 32,
-                                  (n_chunks + kTileChunks - 1) / kTileChunks};
+                                  (n_chunks + kTileChunks - 1) / kTileChunks, a.reverse};
   if (tid == 0) P.prologue();
 
   StatAcc acc;
-  for (int64_t k = 0; P.tile_of(k) < P.ntiles; ++k) {
+  for (int64_t k = 0; P.has(k); ++k) {
     const int64_t tile = P.tile_of(k);
     if (!P.wait(k)) s_abort = 1;
+    float tpart = 0.0f;  // in-range chunk sums of squares of this tile
     const uint32_t stage = P.stage(k);
 #pragma unroll
     for (int c = 0; c < kCPT; ++c) {
@@ -285,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 3) quant4_pipe_kernel(Q4Args a) {
       uint64_t vp[NP];
       bool mul_exact = false;  // MXFP4: decode(q) * s exact, e = fma(-q, s, x)
       if constexpr (FMT == QZ_MXFP4) {
-        const int kexp = UNIT ? 0 : mx_exponent(div6(A), a.scale_round);
+        const int kexp = UNIT ? 0 : mx_exponent(div6(A), SR);
         scode = static_cast<uint32_t>(kexp + 127);
         s = exp2_pos(kexp);
         const float inv = exp2_neg(kexp);
@@ -297,7 +300,15 @@ __global__ void __launch_bounds__(kThreads, 3) quant4_pipe_kernel(Q4Args a) {
         if constexpr (UNIT) {
           scode = 0x38u;
         } else {
-          scode = nv_block_code(div_scalar(div6(A), sg, rg), a.scale_round);
+          const float a6 = div6(A);  // (block_amax / 6) / s_global
+          float t;
+          if (a6 >= 0x1p-100f && sg_fast) {
+            t = div_pos(a6, sg, rg);
+            if (t < 0x1p-120f) t = __fdiv_rn(a6, sg);
+          } else {
+            t = __fdiv_rn(a6, sg);
+          }
+          scode = nv_block_code(t, SR);
         }
         const float2 sr = tab[scode];
         s = sr.x;
@@ -349,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 3) quant4_pipe_kernel(Q4Args a) {
 #pragma unroll
         for (int p = 0; p < NP; ++p) {
           const uint64_t q2 = f16x2_to_f32x2(h[p / 4][p % 4]);
-          e2[p] = mul_exact ? fma2(q2, ns2, xp[p]) : sub2(xp[p], mul2(q2, s2));
+          e2[p] = mul_exact ? fma2(q2, ns2, xp[p]) : sub2(xp[p], mul2_rounded(q2, s2));
           part2 = fma2(e2[p], e2[p], part2);
           float e0, e1;
           upk(e2[p], e0, e1);
@@ -359,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 3) quant4_pipe_kernel(Q4Args a) {
         if (cm <= 0x1p40f && (cm >= 0x1p-40f || cm == 0.0f)) {
           float p0, p1;
           upk(part2, p0, p1);
-          acc_add_sum(acc, __fadd_rn(p0, p1));
+          tpart = __fadd_rn(tpart, __fadd_rn(p0, p1));  // <= 2 * 16 * 2^80: no overflow
         } else {
           double d = 0.0;
 #pragma unroll
@@ -395,6 +406,7 @@ __global__ void __launch_bounds__(kThreads, 3) quant4_pipe_kernel(Q4Args a) {
         }
       }
     }
+    if constexpr (STATS) acc_add_sum(acc, tpart);
     __syncthreads();  // every thread is done with this stage
     if (s_abort) {
       if (tid == 0) {
@@ -410,20 +422,14 @@ __global__ void __launch_bounds__(kThreads, 3) quant4_pipe_kernel(Q4Args a) {
 
 template <int FMT, int DT, bool UNIT, bool STATS>
 qz_status run_pipe(const Q4Args& args, cudaStream_t s) {
-  auto kern = &quant4_pipe_kernel<FMT, DT, UNIT, STATS>;
+  auto kern = args.scale_round == QZ_SCALE_NEAREST ? &quant4_pipe_kernel<FMT, DT, UNIT, STATS, QZ_SCALE_NEAREST>
+                                                    : &quant4_pipe_kernel<FMT, DT, UNIT, STATS, QZ_SCALE_UP>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(kPipeSmem)) != cudaSuccess)
     return QZ_ERR_CUDA;
-  int dev = 0, sms = 1, occ = 1;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, kPipeSmem);
-  const int64_t tiles = (args.g.n_chunks + kTileChunks - 1) / kTileChunks;
-  int64_t grid = static_cast<int64_t>(sms) * (occ < 1 ? 1 : occ);
-  if (tiles < grid) grid = tiles;
-  if (grid < 1) grid = 1;
-  if (grid > kMaxCtas) grid = kMaxCtas;
-  kern<<<static_cast<int>(grid), kThreads, kPipeSmem, s>>>(args);
+  const int grid = grid_for(reinterpret_cast<const void*>(kern),
+                            (args.g.n_chunks + kTileChunks - 1) / kTileChunks, s, kPipeSmem);
+  kern<<<grid, kThreads, kPipeSmem, s>>>(args);
   return launch_status();
 }
 
@@ -472,6 +478,9 @@ qz_status launch_quant4(const qz_desc& d, const void* x, void* codes, void* scal
   args.stats = stats;
   args.ws = ws;
   args.scale_round = d.scale_round;
+  // NVFP4 with a per-tensor scale is normally preceded by a full read of x for its amax;
+  // starting from the end of x picks up what that read left in L2
+  args.reverse = d.format == QZ_NVFP4 && d.granularity == QZ_GRAN_BLOCK;
   const bool unit = d.granularity == QZ_GRAN_UNIT;
   const bool st = stats != nullptr;
   if (d.format == QZ_MXFP4)
