@@ -40,13 +40,13 @@ __device__ __forceinline__ uint64_t fma2_rm(uint64_t a, uint64_t b, uint64_t c) 
   return d;
 }
 
-// fl32(a * b) for both lanes as an fma with a -0 addend.  A separate mul.rn.f32x2 whose
-// result feeds a sub.rn.f32x2 can be contracted into one fma by the assembler, which skips
-// the rounding of the product; an fma cannot be merged further.
-__device__ __forceinline__ uint64_t mul2_rounded(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(0x8000000080000000ull));
-  return d;
+// fl32(a * b) for both lanes as an fma whose addend z2 is a zero the assembler cannot see
+// (a kernel argument).  A mul.rn.f32x2 feeding a sub.rn.f32x2 -- or an fma with a literal
+// zero addend, which is folded into a multiply -- can be contracted into one fma, skipping
+// the rounding of the product; an fma with an opaque addend cannot.  RN(a*b + 0) = RN(a*b),
+// up to the sign of an exact zero product, which no error statistic observes.
+__device__ __forceinline__ uint64_t mul2_rounded(uint64_t a, uint64_t b, uint64_t z2) {
+  return fma2(a, b, z2);
 }
 
 // fl32(x / s) for both lanes from r = RN(1/s) and ns = -s (the FMA-corrected quotient of

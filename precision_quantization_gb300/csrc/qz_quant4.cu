@@ -27,6 +27,7 @@ struct Q4Args {
   void* ws;
   int scale_round;
   bool reverse;  // pipelined path: walk the tiles from the end of the tensor
+  float zero;    // 0.0f, opaque to the assembler (see mul2_rounded)
 };
 
 // fl32(a / b) for scalar scale arithmetic: the FMA-corrected quotient where it is exact
@@ -202,12 +203,214 @@ constexpr int kTileChunks = kPipeTileChunks;
 constexpr int kTileBytes = kPipeTileBytes;
 constexpr int kStages = kPipeStages;
 
-template <int FMT, int DT, bool UNIT, bool STATS, int SR>
-__global__ void __launch_bounds__(kThreads, 3) quant4_pipe_kernel(Q4Args a) {
+template <int NP>
+struct PairsF32 {
+  uint64_t v[NP];
+};
+
+// Sum of squares of one chunk in fp64: only for chunks whose largest |e| lies outside
+// [2^-40, 2^40], where the fp32 squares could overflow or flush to zero.  Kept out of line
+// so the common path carries none of its instructions.
+template <int NP>
+__device__ __noinline__ double sumsq_f64(PairsF32<NP> e) {
+  double d = 0.0;
+#pragma unroll
+  for (int p = 0; p < NP; ++p) {
+    float e0, e1;
+    upk(e.v[p], e0, e1);
+    d = fma(static_cast<double>(e0), static_cast<double>(e0), d);
+    d = fma(static_cast<double>(e1), static_cast<double>(e1), d);
+  }
+  return d;
+}
+
+// Largest magnitude of 2*NP values held as fp32 pairs, as a tree of 3-input maxima (short
+// dependency chains); NAN_PROP selects the NaN-propagating maximum.
+template <int NP, bool NAN_PROP>
+__device__ __forceinline__ float pairs_absmax(const uint64_t (&xp)[NP]) {
+  float v[2 * NP];
+#pragma unroll
+  for (int p = 0; p < NP; ++p) upk(xp[p], v[2 * p], v[2 * p + 1]);
+  float t[(2 * NP + 2) / 3];
+#pragma unroll
+  for (int i = 0; i < (2 * NP + 2) / 3; ++i) {
+    const float a0 = v[3 * i];
+    const float a1 = 3 * i + 1 < 2 * NP ? v[3 * i + 1] : 0.0f;
+    const float a2 = 3 * i + 2 < 2 * NP ? v[3 * i + 2] : 0.0f;
+    t[i] = NAN_PROP ? absmax3(fabsf(a0), a1, a2) : max3(fabsf(a0), fabsf(a1), fabsf(a2));
+  }
+  constexpr int T = (2 * NP + 2) / 3;
+  float u[(T + 2) / 3];
+#pragma unroll
+  for (int i = 0; i < (T + 2) / 3; ++i) {
+    const float a0 = t[3 * i];
+    const float a1 = 3 * i + 1 < T ? t[3 * i + 1] : 0.0f;
+    const float a2 = 3 * i + 2 < T ? t[3 * i + 2] : 0.0f;
+    u[i] = NAN_PROP ? absmax3(a0, a1, a2) : max3(a0, a1, a2);
+  }
+  constexpr int U = (T + 2) / 3;
+  float m = u[0];
+#pragma unroll
+  for (int i = 1; i < U; ++i) m = NAN_PROP ? absmax_nan(m, u[i]) : fmaxf(m, u[i]);
+  return m;
+}
+
+// Per-CTA constants of the pipelined quantizer.
+struct Q4Ctx {
+  float sg, rg;   // NVFP4 s_global and RN(1/s_global)
+  bool sg_fast;   // s_global inside the FMA-quotient range
+  const float2* tab;
+  float zero;     // opaque 0.0f (see mul2_rounded)
+};
+
+// One 32-byte chunk: block amax, scale, quotients, cast, stores, and (STATS) the error of
+// the chunk.  REL: the exact max |e|/|x| search is still open for this warp (T < 1).
+template <int FMT, int DT, bool UNIT, bool STATS, int SR, bool REL>
+__device__ __forceinline__ void q4_chunk(const Q4Args& a, const Q4Ctx& cx, const uint32_t (&w)[8],
+                                         int64_t u, bool valid, int lane, StatAcc& acc,
+                                         float& tpart) {
   constexpr int EPC = Elem<DT>::kPer32B;
   constexpr int BS = FMT == QZ_MXFP4 ? 32 : 16;
   constexpr int L = BS / EPC;
-  constexpr int NP = EPC / 2;  // fp32 pairs per chunk
+  constexpr int NP = EPC / 2;
+  // widen to fp32 pairs; block amax (NaN propagates)
+  uint64_t xp[NP];
+#pragma unroll
+  for (int p = 0; p < NP; ++p) {
+    if constexpr (DT == QZ_BF16) xp[p] = widen_bf16x2(w[p]);
+    else xp[p] = pk(__uint_as_float(w[2 * p]), __uint_as_float(w[2 * p + 1]));
+  }
+  float A = pairs_absmax<NP, true>(xp);
+  if constexpr (L >= 2) A = absmax_nan(A, __shfl_xor_sync(kFull, A, 1));
+  if constexpr (L >= 4) A = absmax_nan(A, __shfl_xor_sync(kFull, A, 2));
+  if (valid && !is_finite_f(A)) flag_status(a.ws, QZ_FLAG_NONFINITE_INPUT);
+
+  // block scale s and the quotients v = fl32(x / s), as fp32 pairs
+  uint32_t scode;
+  float s;
+  uint64_t vp[NP];
+  bool mul_exact = false;  // MXFP4: decode(q) * 2^k exact, so e = fma(-q, s, x)
+  if constexpr (FMT == QZ_MXFP4) {
+    const int kexp = UNIT ? 0 : mx_exponent(div6(A), SR);
+    scode = static_cast<uint32_t>(kexp + 127);
+    s = exp2_pos(kexp);
+    const float inv = exp2_neg(kexp);
+    const uint64_t inv2 = pk(inv, inv);
+#pragma unroll
+    for (int p = 0; p < NP; ++p) vp[p] = mul2(xp[p], inv2);
+    mul_exact = kexp >= -125 && kexp <= 125;
+  } else {
+    if constexpr (UNIT) {
+      scode = 0x38u;
+    } else {
+      const float a6 = div6(A);  // (block_amax / 6) / s_global
+      float t;
+      if (a6 >= 0x1p-100f && cx.sg_fast) {
+        t = div_pos(a6, cx.sg, cx.rg);
+        if (t < 0x1p-120f) t = __fdiv_rn(a6, cx.sg);
+      } else {
+        t = __fdiv_rn(a6, cx.sg);
+      }
+      scode = nv_block_code(t, SR);
+    }
+    const float2 sr = cx.tab[scode];
+    s = sr.x;
+    if (sr.y != 0.0f && __fmul_rn(A, sr.y) <= 0x1p100f) {
+      const uint64_t r2 = pk(sr.y, sr.y), ns2 = pk(-s, -s);
+#pragma unroll
+      for (int p = 0; p < NP; ++p) vp[p] = div2(xp[p], r2, ns2);
+    } else if (s == 0.0f) {
+      const uint64_t z2 = pk(0.0f, 0.0f);
+#pragma unroll
+      for (int p = 0; p < NP; ++p) vp[p] = mul2(xp[p], z2);  // signed zeros
+    } else {
+#pragma unroll
+      for (int p = 0; p < NP; ++p) {
+        float lo, hi;
+        upk(xp[p], lo, hi);
+        vp[p] = pk(__fdiv_rn(lo, s), __fdiv_rn(hi, s));
+      }
+    }
+  }
+
+  // cast and pack 8 at a time; store the codes and the block scale
+  uint32_t cw[EPC / 8];
+  uint32_t h[EPC / 8][4];
+#pragma unroll
+  for (int g8 = 0; g8 < EPC / 8; ++g8) {
+    float v[8];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) upk(vp[4 * g8 + p], v[2 * p], v[2 * p + 1]);
+    if constexpr (STATS) cw[g8] = e2m1x8(v, h[g8]);
+    else cw[g8] = e2m1x8_codes(v);
+  }
+  if (valid) {
+    uint8_t* cp = a.codes + u * (EPC / 2);
+    if constexpr (EPC == 16) {
+      asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(cp), "r"(cw[0]), "r"(cw[1]) : "memory");
+    } else {
+      asm volatile("st.global.u32 [%0], %1;" ::"l"(cp), "r"(cw[0]) : "memory");
+    }
+    if (lane % L == 0) a.scales[u / L] = static_cast<uint8_t>(scode);
+  }
+  if constexpr (!STATS) return;
+
+  // x^ = fl32(decode(q) * s), e = fl32(x - x^); lanes without data hold x = 0, q = 0
+  PairsF32<NP> e;
+  if (FMT == QZ_MXFP4 && __all_sync(kFull, mul_exact)) {
+    const uint64_t ns2 = pk(-s, -s);
+#pragma unroll
+    for (int p = 0; p < NP; ++p) e.v[p] = fma2(f16x2_to_f32x2(h[p / 4][p % 4]), ns2, xp[p]);
+  } else {
+    const uint64_t s2 = pk(s, s), z2 = pk(cx.zero, cx.zero);
+#pragma unroll
+    for (int p = 0; p < NP; ++p)
+      e.v[p] = sub2(xp[p], mul2_rounded(f16x2_to_f32x2(h[p / 4][p % 4]), s2, z2));
+  }
+  const float cm = pairs_absmax<NP, false>(e.v);
+  acc.max_abs = fmaxf(acc.max_abs, cm);
+  if (cm <= 0x1p40f && (cm >= 0x1p-40f || cm == 0.0f)) {
+    // every e^2 <= 2^80 and the chunk sum >= 2^-80: no overflow, and the squares that
+    // underflow (|e| < 2^-75) are below 2^-70 of the chunk's largest
+    uint64_t pa = mul2(e.v[0], e.v[0]), pb = mul2(e.v[1], e.v[1]);
+#pragma unroll
+    for (int p = 2; p < NP; p += 2) {
+      pa = fma2(e.v[p], e.v[p], pa);
+      pb = fma2(e.v[p + 1], e.v[p + 1], pb);
+    }
+    float p0, p1, p2, p3;
+    upk(pa, p0, p1);
+    upk(pb, p2, p3);
+    tpart = __fadd_rn(tpart, __fadd_rn(__fadd_rn(p0, p1), __fadd_rn(p2, p3)));
+  } else {
+    acc.d += sumsq_f64<NP>(e);
+  }
+  if constexpr (REL) {  // see rel_candidate
+    bool cand = false;
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+      float x0, x1, e0, e1;
+      upk(xp[p], x0, x1);
+      upk(e.v[p], e0, e1);
+      cand |= rel_candidate(acc.T, x0, fabsf(e0)) | rel_candidate(acc.T, x1, fabsf(e1));
+    }
+    if (__any_sync(kFull, cand)) {
+      if (cand) {
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+          float x0, x1, e0, e1;
+          upk(xp[p], x0, x1);
+          upk(e.v[p], e0, e1);
+          acc.rel = max3(acc.rel, rel_exact(x0, fabsf(e0)), rel_exact(x1, fabsf(e1)));
+        }
+      }
+      acc.T = warp_max(acc.rel);
+    }
+  }
+}
+
+template <int FMT, int DT, bool UNIT, bool STATS, int SR>
+__global__ void __launch_bounds__(kThreads, 3) quant4_pipe_kernel(Q4Args a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[kStages];
   __shared__ float2 tab[128];  // NVFP4: (s, RN(1/s)) for every E4M3 block code
@@ -215,24 +418,23 @@ __global__ void __launch_bounds__(kThreads, 3) quant4_pipe_kernel(Q4Args a) {
   const int tid = threadIdx.x, lane = tid & 31;
   const int64_t n_chunks = a.g.n_chunks;
 
-  float sg = 1.0f, rg = 1.0f;
-  bool sg_fast = true;
+  Q4Ctx cx{1.0f, 1.0f, true, tab, a.zero};
   if constexpr (FMT == QZ_NVFP4) {
     if constexpr (!UNIT) {
       const float alpha = *a.amax;
       if ((!(alpha >= 0.0f) || !is_finite_f(alpha)) && blockIdx.x == 0 && tid == 0)
         flag_status(a.ws, QZ_FLAG_BAD_AMAX);
-      sg = __fdiv_rn(alpha, 2688.0f);  // global_amax / (6 * 448)
-      if (sg == 0.0f) sg = 1.0f;
-      rg = __frcp_rn(sg);
+      cx.sg = __fdiv_rn(alpha, 2688.0f);  // global_amax / (6 * 448)
+      if (cx.sg == 0.0f) cx.sg = 1.0f;
+      cx.rg = __frcp_rn(cx.sg);
     }
-    sg_fast = fast_div_ok(sg);
+    cx.sg_fast = fast_div_ok(cx.sg);
     for (int c = tid; c < 128; c += kThreads) {
-      const float s = __fmul_rn(sg, dec_e4m3(static_cast<uint32_t>(c)));
+      const float s = __fmul_rn(cx.sg, dec_e4m3(static_cast<uint32_t>(c)));
       tab[c] = make_float2(s, (s > 0.0f && fast_div_ok(s)) ? __frcp_rn(s) : 0.0f);
     }
   }
-  if (a.tscale_out && blockIdx.x == 0 && tid == 0) *a.tscale_out = sg;
+  if (a.tscale_out && blockIdx.x == 0 && tid == 0) *a.tscale_out = cx.sg;
   if (tid == 0) {
     for (int i = 0; i < kStages; ++i) mbar_init(smem_addr(&bars[i]), 1);
     mbar_init_fence();
@@ -262,149 +464,10 @@ __global__ void __launch_bounds__(kThreads, 3) quant4_pipe_kernel(Q4Args a) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) w[i] = 0u;
       }
-      // widen to fp32 pairs; block amax (NaN propagates)
-      uint64_t xp[NP];
-      float A = 0.0f;
-#pragma unroll
-      for (int p = 0; p < NP; ++p) {
-        float lo, hi;
-        if constexpr (DT == QZ_BF16) {
-          lo = __uint_as_float(w[p] << 16);
-          hi = __uint_as_float(w[p] & 0xffff0000u);
-        } else {
-          lo = __uint_as_float(w[2 * p]);
-          hi = __uint_as_float(w[2 * p + 1]);
-        }
-        xp[p] = pk(lo, hi);
-        A = absmax3(A, lo, hi);
-      }
-      if constexpr (L >= 2) A = absmax_nan(A, __shfl_xor_sync(kFull, A, 1));
-      if constexpr (L >= 4) A = absmax_nan(A, __shfl_xor_sync(kFull, A, 2));
-      if (valid && !is_finite_f(A)) flag_status(a.ws, QZ_FLAG_NONFINITE_INPUT);
-
-      // block scale s and the quotients v = fl32(x / s), as fp32 pairs
-      uint32_t scode;
-      float s;
-      uint64_t vp[NP];
-      bool mul_exact = false;  // MXFP4: decode(q) * s exact, e = fma(-q, s, x)
-      if constexpr (FMT == QZ_MXFP4) {
-        const int kexp = UNIT ? 0 : mx_exponent(div6(A), SR);
-        scode = static_cast<uint32_t>(kexp + 127);
-        s = exp2_pos(kexp);
-        const float inv = exp2_neg(kexp);
-        const uint64_t inv2 = pk(inv, inv);
-#pragma unroll
-        for (int p = 0; p < NP; ++p) vp[p] = mul2(xp[p], inv2);
-        mul_exact = kexp >= -125 && kexp <= 125;
-      } else {
-        if constexpr (UNIT) {
-          scode = 0x38u;
-        } else {
-          const float a6 = div6(A);  // (block_amax / 6) / s_global
-          float t;
-          if (a6 >= 0x1p-100f && sg_fast) {
-            t = div_pos(a6, sg, rg);
-            if (t < 0x1p-120f) t = __fdiv_rn(a6, sg);
-          } else {
-            t = __fdiv_rn(a6, sg);
-          }
-          scode = nv_block_code(t, SR);
-        }
-        const float2 sr = tab[scode];
-        s = sr.x;
-        if (sr.y != 0.0f && __fmul_rn(A, sr.y) <= 0x1p100f) {
-          const uint64_t r2 = pk(sr.y, sr.y), ns2 = pk(-s, -s);
-#pragma unroll
-          for (int p = 0; p < NP; ++p) vp[p] = div2(xp[p], r2, ns2);
-        } else if (s == 0.0f) {
-          const uint64_t z2 = pk(0.0f, 0.0f);
-#pragma unroll
-          for (int p = 0; p < NP; ++p) vp[p] = mul2(xp[p], z2);  // signed zeros
-        } else {
-#pragma unroll
-          for (int p = 0; p < NP; ++p) {
-            float lo, hi;
-            upk(xp[p], lo, hi);
-            vp[p] = pk(__fdiv_rn(lo, s), __fdiv_rn(hi, s));
-          }
-        }
-      }
-
-      // cast and pack 8 at a time; store the codes and the block scale
-      uint32_t cw[EPC / 8];
-      uint32_t h[EPC / 8][4];
-#pragma unroll
-      for (int g8 = 0; g8 < EPC / 8; ++g8) {
-        float v[8];
-#pragma unroll
-        for (int p = 0; p < 4; ++p) upk(vp[4 * g8 + p], v[2 * p], v[2 * p + 1]);
-        if constexpr (STATS) cw[g8] = e2m1x8(v, h[g8]);
-        else cw[g8] = e2m1x8_codes(v);
-      }
-      if (valid) {
-        uint8_t* cp = a.codes + u * (EPC / 2);
-        if constexpr (EPC == 16) {
-          asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(cp), "r"(cw[0]), "r"(cw[1]) : "memory");
-        } else {
-          asm volatile("st.global.u32 [%0], %1;" ::"l"(cp), "r"(cw[0]) : "memory");
-        }
-        if (lane % L == 0) a.scales[u / L] = static_cast<uint8_t>(scode);
-      }
-
-      if constexpr (STATS) {
-        // x^ = fl32(decode(q) * s), e = fl32(x - x^); lanes without data hold x = 0, q = 0
-        const uint64_t s2 = pk(s, s), ns2 = pk(-s, -s);
-        uint64_t e2[NP];
-        uint64_t part2 = pk(0.0f, 0.0f);
-        float cm = 0.0f;
-#pragma unroll
-        for (int p = 0; p < NP; ++p) {
-          const uint64_t q2 = f16x2_to_f32x2(h[p / 4][p % 4]);
-          e2[p] = mul_exact ? fma2(q2, ns2, xp[p]) : sub2(xp[p], mul2_rounded(q2, s2));
-          part2 = fma2(e2[p], e2[p], part2);
-          float e0, e1;
-          upk(e2[p], e0, e1);
-          cm = max3(cm, fabsf(e0), fabsf(e1));
-        }
-        acc.max_abs = fmaxf(acc.max_abs, cm);
-        if (cm <= 0x1p40f && (cm >= 0x1p-40f || cm == 0.0f)) {
-          float p0, p1;
-          upk(part2, p0, p1);
-          tpart = __fadd_rn(tpart, __fadd_rn(p0, p1));  // <= 2 * 16 * 2^80: no overflow
-        } else {
-          double d = 0.0;
-#pragma unroll
-          for (int p = 0; p < NP; ++p) {
-            float e0, e1;
-            upk(e2[p], e0, e1);
-            d = fma(static_cast<double>(e0), static_cast<double>(e0), d);
-            d = fma(static_cast<double>(e1), static_cast<double>(e1), d);
-          }
-          acc.d += d;
-        }
-        if (acc.T < 1.0f) {  // warp-uniform; see rel_candidate
-          bool cand = false;
-#pragma unroll
-          for (int p = 0; p < NP; ++p) {
-            float x0, x1, e0, e1;
-            upk(xp[p], x0, x1);
-            upk(e2[p], e0, e1);
-            cand |= rel_candidate(acc.T, x0, fabsf(e0)) | rel_candidate(acc.T, x1, fabsf(e1));
-          }
-          if (__any_sync(kFull, cand)) {
-            if (cand) {
-#pragma unroll
-              for (int p = 0; p < NP; ++p) {
-                float x0, x1, e0, e1;
-                upk(xp[p], x0, x1);
-                upk(e2[p], e0, e1);
-                acc.rel = max3(acc.rel, rel_exact(x0, fabsf(e0)), rel_exact(x1, fabsf(e1)));
-              }
-            }
-            acc.T = warp_max(acc.rel);
-          }
-        }
-      }
+      if (!STATS || acc.T >= 1.0f)  // warp-uniform: the relative-error search is settled
+        q4_chunk<FMT, DT, UNIT, STATS, SR, false>(a, cx, w, u, valid, lane, acc, tpart);
+      else
+        q4_chunk<FMT, DT, UNIT, STATS, SR, true>(a, cx, w, u, valid, lane, acc, tpart);
     }
     if constexpr (STATS) acc_add_sum(acc, tpart);
     __syncthreads();  // every thread is done with this stage
@@ -481,6 +544,7 @@ qz_status launch_quant4(const qz_desc& d, const void* x, void* codes, void* scal
   // NVFP4 with a per-tensor scale is normally preceded by a full read of x for its amax;
   // starting from the end of x picks up what that read left in L2
   args.reverse = d.format == QZ_NVFP4 && d.granularity == QZ_GRAN_BLOCK;
+  args.zero = 0.0f;
   const bool unit = d.granularity == QZ_GRAN_UNIT;
   const bool st = stats != nullptr;
   if (d.format == QZ_MXFP4)
