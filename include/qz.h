@@ -173,6 +173,27 @@ QZ_API qz_status qz_error_stats(const qz_desc* desc, const void* x, const void* 
                          const void* scales, const float* tensor_scale_dev,
                          qz_stats* stats_dev, void* ws, qz_stream_t stream);
 
+/* qz_error_stats without a workspace argument, for callers that cannot allocate device
+ * memory (code running under another framework's memory pool, paths on which cudaMalloc /
+ * cudaFree and their device synchronisation are not allowed, plugins handed only their
+ * input and output buffers).  The post has no counterpart; this is an interface matter.
+ * Same arguments, results and errors as qz_error_stats otherwise.
+ *   Scratch: a fixed array of qz_workspace_size() bytes (82 176 in this version) in device
+ *   memory, part of the library module: every GPU that loads the library holds it until
+ *   the process exits.  The statistics need no more scratch for larger tensors; a
+ *   descriptor whose workspace would exceed the array is rejected with QZ_ERR_WORKSPACE.
+ *   Allocation: none -- no cudaMalloc, cudaFree or allocating library call.
+ *   First call on a device: looks up the array's device address (cudaGetSymbolAddress,
+ *   with that device current) and caches it; make that first call before any stream
+ *   capture on the device.
+ *   Sharing: every call on a device uses the same array, which keeps what the previous
+ *   call left; each call clears its counters behind its kernel on `stream`.  Calls that
+ *   overlap on the GPU (different streams, no ordering between them) race on the array and
+ *   give wrong statistics. */
+QZ_API qz_status qz_error_stats_noalloc(const qz_desc* desc, const void* x, const void* codes,
+                                        const void* scales, const float* tensor_scale_dev,
+                                        qz_stats* stats_dev, qz_stream_t stream);
+
 /* Synchronize `stream`, then copy the workspace status word (QZ_FLAG_* bits, sticky until
  * qz_workspace_init) into *flags_host. */
 QZ_API qz_status qz_get_device_status(const void* ws, uint32_t* flags_host, qz_stream_t stream);

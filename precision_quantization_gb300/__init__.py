@@ -38,7 +38,8 @@ BLOCK_SIZE = {QZ_MXFP4: 32, QZ_NVFP4: 16}
 
 # Names of the exported C symbols (the whole ABI of include/qz.h).
 ABI_SYMBOLS = ("qz_status_string", "qz_workspace_size", "qz_workspace_init", "qz_amax",
-               "qz_quantize", "qz_dequantize", "qz_error_stats", "qz_get_device_status")
+               "qz_quantize", "qz_dequantize", "qz_error_stats", "qz_error_stats_noalloc",
+               "qz_get_device_status")
 
 
 class QzDesc(C.Structure):
@@ -81,6 +82,7 @@ def lib():
             "qz_quantize": (i32, [dp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "qz_dequantize": (i32, [dp, vp, vp, vp, vp, i32, vp]),
             "qz_error_stats": (i32, [dp, vp, vp, vp, vp, vp, vp, vp]),
+            "qz_error_stats_noalloc": (i32, [dp, vp, vp, vp, vp, vp, vp]),
             "qz_get_device_status": (i32, [vp, C.POINTER(C.c_uint32), vp]),
         }
         for name, (res, args) in sig.items():
@@ -125,6 +127,14 @@ def qz_error_stats(desc: QzDesc, x: int, codes: int, scales: int | None,
                    stream: int = 0) -> int:
     return lib().qz_error_stats(C.byref(desc), x, codes, scales, tensor_scale_dev, stats_dev,
                                 ws, stream)
+
+
+def qz_error_stats_noalloc(desc: QzDesc, x: int, codes: int, scales: int | None,
+                           tensor_scale_dev: int | None, stats_dev: int, stream: int = 0) -> int:
+    """qz_error_stats for callers that cannot allocate: no workspace argument (the library
+    uses a fixed scratch array of its own; see include/qz.h)."""
+    return lib().qz_error_stats_noalloc(C.byref(desc), x, codes, scales, tensor_scale_dev,
+                                        stats_dev, stream)
 
 
 def qz_get_device_status(ws: int, stream: int = 0) -> tuple[int, int]:
