@@ -117,6 +117,104 @@ __device__ __forceinline__ uint64_t f16x2_to_f32x2(uint32_t h) {
   return r;
 }
 
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+template <int NP>
+struct Pairs {
+  uint64_t v[NP];
+};
+
+// Sum of squares of 2*NP errors in fp64 -- only for chunks whose largest |e| lies outside
+// [2^-40, 2^40], where fp32 squares could overflow or flush to zero.  Out of line, so the
+// common path carries none of its instructions.
+template <int NP>
+__device__ __noinline__ double pairs_sumsq_f64(Pairs<NP> e) {
+  double d = 0.0;
+#pragma unroll
+  for (int p = 0; p < NP; ++p) {
+    float e0, e1;
+    upk(e.v[p], e0, e1);
+    d = fma(static_cast<double>(e0), static_cast<double>(e0), d);
+    d = fma(static_cast<double>(e1), static_cast<double>(e1), d);
+  }
+  return d;
+}
+
+// Largest |value| of 2*NP values held as fp32 pairs: a tree of 3-input maxima.
+template <int NP>
+__device__ __forceinline__ float pairs_max_abs(const uint64_t (&p2)[NP]) {
+  float v[2 * NP];
+#pragma unroll
+  for (int p = 0; p < NP; ++p) upk(p2[p], v[2 * p], v[2 * p + 1]);
+  constexpr int T = (2 * NP + 2) / 3;
+  float t[T];
+#pragma unroll
+  for (int i = 0; i < T; ++i) {
+    const float a1 = 3 * i + 1 < 2 * NP ? fabsf(v[3 * i + 1]) : 0.0f;
+    const float a2 = 3 * i + 2 < 2 * NP ? fabsf(v[3 * i + 2]) : 0.0f;
+    t[i] = max3(fabsf(v[3 * i]), a1, a2);
+  }
+  float m = t[0];
+#pragma unroll
+  for (int i = 1; i + 1 < T; i += 2) m = max3(m, t[i], t[i + 1]);
+  if constexpr (T % 2 == 0) m = fmaxf(m, t[T - 1]);
+  return m;
+}
+
+// Accumulate the errors e (fp32 pairs) of one chunk whose inputs are x: largest |e| and
+// sum of e^2 (into tpart when every |e| lies in [2^-40, 2^40], else in fp64), and -- REL,
+// while the warp's exact max |e|/|x| search is open -- the candidates of rel_candidate.
+// Every lane of the warp must make the same calls (the REL part votes).
+template <int NP, bool REL>
+__device__ __forceinline__ void acc_pairs(StatAcc& acc, const uint64_t (&xp)[NP], const Pairs<NP>& e,
+                                          float& tpart) {
+  const float cm = pairs_max_abs<NP>(e.v);
+  acc.max_abs = fmaxf(acc.max_abs, cm);
+  if (cm <= 0x1p40f && (cm >= 0x1p-40f || cm == 0.0f)) {
+    // every e^2 <= 2^80 and the chunk sum >= 2^-80: no overflow, and the squares that
+    // underflow (|e| < 2^-75) are below 2^-70 of the chunk's largest
+    uint64_t pa = mul2(e.v[0], e.v[0]);
+    uint64_t pb = NP > 1 ? mul2(e.v[NP > 1 ? 1 : 0], e.v[NP > 1 ? 1 : 0]) : pk(0.0f, 0.0f);
+#pragma unroll
+    for (int p = 2; p < NP; p += 2) {
+      pa = fma2(e.v[p], e.v[p], pa);
+      if (p + 1 < NP) pb = fma2(e.v[p + 1], e.v[p + 1], pb);
+    }
+    float p0, p1, p2, p3;
+    upk(pa, p0, p1);
+    upk(pb, p2, p3);
+    tpart = __fadd_rn(tpart, __fadd_rn(__fadd_rn(p0, p1), __fadd_rn(p2, p3)));
+  } else {
+    acc.d += pairs_sumsq_f64<NP>(e);
+  }
+  if constexpr (REL) {  // see rel_candidate
+    bool cand = false;
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+      float x0, x1, e0, e1;
+      upk(xp[p], x0, x1);
+      upk(e.v[p], e0, e1);
+      cand |= rel_candidate(acc.T, x0, fabsf(e0)) | rel_candidate(acc.T, x1, fabsf(e1));
+    }
+    if (__any_sync(kFull, cand)) {
+      if (cand) {
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+          float x0, x1, e0, e1;
+          upk(xp[p], x0, x1);
+          upk(e.v[p], e0, e1);
+          acc.rel = max3(acc.rel, rel_exact(x0, fabsf(e0)), rel_exact(x1, fabsf(e1)));
+        }
+      }
+      acc.T = warp_max(acc.rel);
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------------------
 // mbarrier + bulk copy global -> shared
 // ---------------------------------------------------------------------------------------

@@ -8,6 +8,7 @@
 // its amax reduced across the CTA, and the codes produced from the registers.
 #include "qz_device.cuh"
 #include "qz_internal.h"
+#include "qz_pipe.cuh"
 
 namespace qz {
 namespace {
@@ -243,6 +244,318 @@ __global__ void __launch_bounds__(kThreads) quant8_row_kernel(Q8Args a) {
   if constexpr (STATS) stats_finish(acc, a.ws, a.stats, static_cast<uint64_t>(g.rows * g.cols));
 }
 
+// ---------------------------------------------------------------------------------------
+// Staged (shared-memory) paths, see qz_pipe.cuh
+// ---------------------------------------------------------------------------------------
+constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23: fl(v + kMagic) - kMagic = RNE(v), |v| < 2^22
+
+// Cast the quotients of one chunk (NP fp32 pairs) to codes.  Writes the EPC code bytes
+// (element 0 in the lowest byte of cw[0]) and, with STATS, the code values q as fp32 pairs.
+// INT8 rounds with the magic-number addition, which leaves RNE(v) in the low byte of the
+// sum's bits and needs no float-to-int conversion; CLAMP limits v to [-127, 127] first
+// (only needed when |v| can exceed 127.5: a supplied amax or the unit scale).
+template <int FMT, int NP, bool STATS, bool CLAMP>
+__device__ __forceinline__ void q8_cast(const uint64_t (&vp)[NP], uint32_t (&cw)[NP / 2],
+                                        uint64_t (&qf)[NP]) {
+  if constexpr (FMT == QZ_INT8) {
+    const uint64_t m2 = pk(kMagic, kMagic);
+    uint32_t lo[NP], hi[NP];
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+      uint64_t v2 = vp[p];
+      if constexpr (CLAMP) {
+        float a, b;
+        upk(v2, a, b);
+        v2 = pk(fminf(fmaxf(a, -127.0f), 127.0f), fminf(fmaxf(b, -127.0f), 127.0f));
+      }
+      const uint64_t t2 = add2(v2, m2);
+      if constexpr (STATS) qf[p] = sub2(t2, m2);
+      float tl, th;
+      upk(t2, tl, th);
+      lo[p] = __float_as_uint(tl);
+      hi[p] = __float_as_uint(th);
+    }
+#pragma unroll
+    for (int p = 0; p < NP; p += 2) {
+      const uint32_t u01 = __byte_perm(lo[p], hi[p], 0x0040);
+      const uint32_t u23 = __byte_perm(lo[p + 1], hi[p + 1], 0x0040);
+      cw[p / 2] = __byte_perm(u01, u23, 0x5410);
+    }
+  } else {
+    uint32_t h16[NP];
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+      float a, b;
+      upk(vp[p], a, b);
+      h16[p] = cvt8x2<FMT>(a, b);
+      if constexpr (STATS) {
+        uint32_t hh;
+        const uint16_t c = static_cast<uint16_t>(h16[p]);
+        if constexpr (FMT == QZ_FP8_E4M3) asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hh) : "h"(c));
+        else asm("cvt.rn.f16x2.e5m2x2 %0, %1;" : "=r"(hh) : "h"(c));
+        qf[p] = f16x2_to_f32x2(hh);
+      }
+    }
+#pragma unroll
+    for (int p = 0; p < NP; p += 2) cw[p / 2] = (h16[p] & 0xffffu) | (h16[p + 1] << 16);
+  }
+}
+
+// One chunk of the per-tensor / unit-scale path: quotients, cast, store, stats.
+template <int FMT, int DT, int MODE, bool STATS, bool REL>
+__device__ __forceinline__ void q8_chunk(const uint32_t (&w)[8], bool valid, uint8_t* cp, float s,
+                                         uint64_t r2, uint64_t ns2, uint64_t s2, uint64_t z2, bool fast,
+                                         void* ws, StatAcc& acc, float& tpart) {
+  constexpr int EPC = Elem<DT>::kPer32B;
+  constexpr int NP = EPC / 2;
+  uint64_t xp[NP];
+#pragma unroll
+  for (int p = 0; p < NP; ++p) {
+    if constexpr (DT == QZ_BF16) xp[p] = widen_bf16x2(w[p]);
+    else xp[p] = pk(__uint_as_float(w[2 * p]), __uint_as_float(w[2 * p + 1]));
+  }
+  bool f = fast;
+  if constexpr (MODE != kTensorComputed) {
+    // no earlier pass has looked at these values: check finiteness here, and keep the FMA
+    // quotient only where |x| / s cannot overflow (a supplied amax may be too small)
+    float A = 0.0f;
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+      float a, b;
+      upk(xp[p], a, b);
+      A = absmax3(A, a, b);
+    }
+    if (valid && !is_finite_f(A)) flag_status(ws, QZ_FLAG_NONFINITE_INPUT);
+    if constexpr (MODE == kTensorSupplied) {
+      float r, rr;
+      upk(r2, r, rr);
+      f = f && (__fmul_rn(A, r) <= 0x1p100f);
+    }
+  }
+  uint64_t vp[NP];
+  if constexpr (MODE == kUnit) {
+#pragma unroll
+    for (int p = 0; p < NP; ++p) vp[p] = xp[p];
+  } else {
+    if (f) {
+#pragma unroll
+      for (int p = 0; p < NP; ++p) vp[p] = div2(xp[p], r2, ns2);
+    } else {
+#pragma unroll
+      for (int p = 0; p < NP; ++p) {
+        float a, b;
+        upk(xp[p], a, b);
+        vp[p] = pk(__fdiv_rn(a, s), __fdiv_rn(b, s));
+      }
+    }
+  }
+  uint32_t cw[NP / 2];
+  uint64_t qf[NP];
+  q8_cast<FMT, NP, STATS, MODE != kTensorComputed>(vp, cw, qf);
+  if (valid) {
+    if constexpr (EPC == 16) {
+      asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(cp), "r"(cw[0]), "r"(cw[1]),
+                   "r"(cw[2]), "r"(cw[3])
+                   : "memory");
+    } else {
+      asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(cp), "r"(cw[0]), "r"(cw[1]) : "memory");
+    }
+  }
+  if constexpr (STATS) {
+    // x^ = fl32(q * s) (= q for the unit scale), e = fl32(x - x^)
+    Pairs<NP> e;
+#pragma unroll
+    for (int p = 0; p < NP; ++p) e.v[p] = sub2(xp[p], MODE == kUnit ? qf[p] : mul2_rounded(qf[p], s2, z2));
+    acc_pairs<NP, REL>(acc, xp, e, tpart);
+  }
+}
+
+// Dense tensors, per-tensor or unit scale: the quant4 pipeline (16 KiB tiles streamed
+// through shared memory by bulk copies, two 32-byte chunks per lane per tile).
+template <int FMT, int DT, int MODE, bool STATS>
+__global__ void __launch_bounds__(kThreads, 3) quant8_pipe_kernel(Q8Args a, float zero) {
+  constexpr int EPC = Elem<DT>::kPer32B;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bars[kPipeStages];
+  __shared__ int s_abort;
+  const int tid = threadIdx.x;
+  const int64_t n_chunks = a.g.n_chunks;
+  float s = 1.0f, r = 1.0f;
+  bool fast = true;
+  if constexpr (MODE != kUnit) {
+    const float alpha = *a.amax;
+    if (MODE == kTensorSupplied && (!(alpha >= 0.0f) || !is_finite_f(alpha)) && blockIdx.x == 0 &&
+        tid == 0)
+      flag_status(a.ws, QZ_FLAG_BAD_AMAX);
+    s = __fdiv_rn(alpha, Fmt8<FMT>::kMax);
+    if (s == 0.0f) s = 1.0f;
+    r = __frcp_rn(s);
+    fast = fast_div_ok(s);
+  }
+  if (a.tscale_out && blockIdx.x == 0 && tid == 0) *a.tscale_out = s;
+  const uint64_t r2 = pk(r, r), ns2 = pk(-s, -s), s2 = pk(s, s), z2 = pk(zero, zero);
+  if (tid == 0) {
+    for (int i = 0; i < kPipeStages; ++i) mbar_init(smem_addr(&bars[i]), 1);
+    mbar_init_fence();
+    s_abort = 0;
+  }
+  __syncthreads();
+  BulkPipe<kPipeStages, kPipeTileBytes> P{smem_addr(smem), smem_addr(&bars[0]),
+                                          static_cast<const char*>(a.x), n_chunks * 32,
+                                          (n_chunks + kPipeTileChunks - 1) / kPipeTileChunks, false};
+  if (tid == 0) P.prologue();
+  StatAcc acc;
+  for (int64_t k = 0; P.has(k); ++k) {
+    const int64_t tile = P.tile_of(k);
+    if (!P.wait(k)) s_abort = 1;
+    float tpart = 0.0f;
+    const uint32_t stage = P.stage(k);
+#pragma unroll
+    for (int c = 0; c < kPipeCPT; ++c) {
+      const int j = c * kThreads + tid;
+      const int64_t u = tile * kPipeTileChunks + j;
+      const bool valid = u < n_chunks;
+      uint32_t w[8];
+      if (valid) {
+        lds32B(w, stage + 32u * j);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = 0u;
+      }
+      uint8_t* cp = a.codes + u * EPC;
+      if (!STATS || acc.T >= 1.0f)  // warp-uniform: the relative-error search is settled
+        q8_chunk<FMT, DT, MODE, STATS, false>(w, valid, cp, s, r2, ns2, s2, z2, fast, a.ws, acc, tpart);
+      else
+        q8_chunk<FMT, DT, MODE, STATS, true>(w, valid, cp, s, r2, ns2, s2, z2, fast, a.ws, acc, tpart);
+    }
+    if constexpr (STATS) acc_add_sum(acc, tpart);
+    __syncthreads();
+    if (s_abort) {
+      if (tid == 0) {
+        flag_status(a.ws, QZ_FLAG_PIPELINE_TIMEOUT);
+        P.drain(k);
+      }
+      return;
+    }
+    if (tid == 0) P.issue(k + kPipeStages);
+  }
+  if constexpr (STATS) stats_finish(acc, a.ws, a.stats, static_cast<uint64_t>(a.g.rows * a.g.cols));
+}
+
+// Per-row scale with rows of at most kRowPipeMaxBytes: each row arrives in shared memory
+// with one bulk copy (two rows in flight per CTA); the row amax and the codes are both
+// computed from shared memory, so x is read from HBM once.
+constexpr int kRowPipeMaxBytes = 64 * 1024;
+
+template <int FMT, int DT, bool STATS>
+__global__ void __launch_bounds__(kThreads) quant8_rowpipe_kernel(Q8Args a, float zero, uint32_t stage_bytes) {
+  constexpr int EPC = Elem<DT>::kPer32B;
+  constexpr int NP = EPC / 2;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bars[2];
+  __shared__ float s_red[kWarps];
+  __shared__ int s_abort;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const Geom& g = a.g;
+  const uint32_t row_bytes = static_cast<uint32_t>(g.cols) * Elem<DT>::kBytes;
+  if (a.tscale_out && blockIdx.x == 0 && tid == 0) *a.tscale_out = 1.0f;
+  if (tid == 0) {
+    mbar_init(smem_addr(&bars[0]), 1);
+    mbar_init(smem_addr(&bars[1]), 1);
+    mbar_init_fence();
+    s_abort = 0;
+  }
+  __syncthreads();
+  const uint32_t base = smem_addr(smem);
+  auto issue = [&](int64_t k) {  // thread 0: row blockIdx.x + k * gridDim.x into stage k % 2
+    const int64_t row = blockIdx.x + k * gridDim.x;
+    if (row >= g.rows) return;
+    const uint32_t st = static_cast<uint32_t>(k & 1), bar = smem_addr(&bars[st]);
+    mbar_expect_tx(bar, row_bytes);
+    bulk_g2s(base + st * stage_bytes, static_cast<const char*>(a.x) + row * g.ld * Elem<DT>::kBytes,
+             row_bytes, bar);
+  };
+  if (tid == 0) {
+    issue(0);
+    issue(1);
+  }
+  const uint64_t z2 = pk(zero, zero);
+  StatAcc acc;
+  for (int64_t k = 0; blockIdx.x + k * gridDim.x < g.rows; ++k) {
+    const int64_t row = blockIdx.x + k * gridDim.x;
+    const uint32_t st = static_cast<uint32_t>(k & 1);
+    if (!mbar_wait(smem_addr(&bars[st]), static_cast<uint32_t>((k >> 1) & 1), kWaitLimitNs)) s_abort = 1;
+    const uint32_t rbase = base + st * stage_bytes;
+    // pass 1: row amax (NaN propagates)
+    float A = 0.0f;
+    for (int64_t j = tid; j < g.cpr; j += kThreads) {
+      uint32_t w[8];
+      lds32B(w, rbase + 32u * static_cast<uint32_t>(j));
+#pragma unroll
+      for (int p = 0; p < NP; ++p) {
+        float lo, hi;
+        if constexpr (DT == QZ_BF16) {
+          lo = __uint_as_float(w[p] << 16);
+          hi = __uint_as_float(w[p] & 0xffff0000u);
+        } else {
+          lo = __uint_as_float(w[2 * p]);
+          hi = __uint_as_float(w[2 * p + 1]);
+        }
+        A = absmax3(A, lo, hi);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) A = absmax_nan(A, __shfl_xor_sync(kFull, A, o));
+    if (lane == 0) s_red[warp] = A;
+    __syncthreads();
+    A = s_red[0];
+#pragma unroll
+    for (int i = 1; i < kWarps; ++i) A = absmax_nan(A, s_red[i]);
+    float s = __fdiv_rn(A, Fmt8<FMT>::kMax);  // alpha / qmax
+    if (s == 0.0f) s = 1.0f;
+    const float r = __frcp_rn(s);
+    const bool fast = fast_div_ok(s);
+    if (tid == 0) {
+      a.scales[row] = s;
+      if (!is_finite_f(A)) flag_status(a.ws, QZ_FLAG_NONFINITE_INPUT);
+    }
+    const uint64_t r2 = pk(r, r), ns2 = pk(-s, -s), s2 = pk(s, s);
+    // pass 2: codes (warp-uniform trip count: the stats vote)
+    float tpart = 0.0f;
+    uint8_t* crow = a.codes + row * g.cols;
+    for (int64_t jb = tid & ~31; jb < g.cpr; jb += kThreads) {
+      const int64_t j = jb + lane;
+      const bool valid = j < g.cpr;
+      uint32_t w[8];
+      if (valid) {
+        lds32B(w, rbase + 32u * static_cast<uint32_t>(j));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = 0u;
+      }
+      if (!STATS || acc.T >= 1.0f)
+        q8_chunk<FMT, DT, kTensorComputed, STATS, false>(w, valid, crow + j * EPC, s, r2, ns2, s2, z2,
+                                                         fast, a.ws, acc, tpart);
+      else
+        q8_chunk<FMT, DT, kTensorComputed, STATS, true>(w, valid, crow + j * EPC, s, r2, ns2, s2, z2,
+                                                        fast, a.ws, acc, tpart);
+    }
+    if constexpr (STATS) acc_add_sum(acc, tpart);
+    __syncthreads();  // stage and s_red free again
+    if (s_abort) {
+      if (tid == 0) {
+        flag_status(a.ws, QZ_FLAG_PIPELINE_TIMEOUT);
+        for (int64_t j = k; j < k + 2; ++j)
+          if (blockIdx.x + j * gridDim.x < g.rows)
+            mbar_wait(smem_addr(&bars[j & 1]), static_cast<uint32_t>((j >> 1) & 1), kWaitLimitNs);
+      }
+      return;
+    }
+    if (tid == 0) issue(k + 2);
+  }
+  if constexpr (STATS) stats_finish(acc, a.ws, a.stats, static_cast<uint64_t>(g.rows * g.cols));
+}
+
 template <typename K>
 qz_status go(K kern, const Q8Args& args, int64_t work_ctas, cudaStream_t s) {
   const int grid = grid_for(reinterpret_cast<const void*>(kern), work_ctas, s);
@@ -254,6 +567,19 @@ template <int FMT, int DT, bool STATS>
 qz_status run_row(const Q8Args& args, cudaStream_t s) {
   const Geom& g = args.g;
   const int64_t rows = g.rows;
+  const int64_t row_bytes = g.cols * Elem<DT>::kBytes;
+  if (g.vec && row_bytes <= kRowPipeMaxBytes && reinterpret_cast<uintptr_t>(args.x) % 16 == 0 &&
+      (g.ld * Elem<DT>::kBytes) % 16 == 0) {
+    auto kern = &quant8_rowpipe_kernel<FMT, DT, STATS>;
+    const uint32_t stage = static_cast<uint32_t>((row_bytes + 127) / 128 * 128);
+    const size_t smem = 2 * static_cast<size_t>(stage);
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess)
+      return QZ_ERR_CUDA;
+    const int grid = grid_for(reinterpret_cast<const void*>(kern), rows, s, smem);
+    kern<<<grid, kThreads, smem, s>>>(args, 0.0f, stage);
+    return launch_status();
+  }
   if (g.vec) {
     if (g.cpr <= kThreads) return go(&quant8_row_kernel<FMT, DT, STATS, true, 1>, args, rows, s);
     if (g.cpr <= 2 * kThreads) return go(&quant8_row_kernel<FMT, DT, STATS, true, 2>, args, rows, s);
@@ -266,6 +592,16 @@ qz_status run_row(const Q8Args& args, cudaStream_t s) {
 
 template <int FMT, int DT, int MODE, bool STATS>
 qz_status run_flat(const Q8Args& args, cudaStream_t s) {
+  if (args.g.vec && args.g.dense && reinterpret_cast<uintptr_t>(args.x) % 16 == 0) {
+    auto kern = &quant8_pipe_kernel<FMT, DT, MODE, STATS>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kPipeSmem)) != cudaSuccess)
+      return QZ_ERR_CUDA;
+    const int grid = grid_for(reinterpret_cast<const void*>(kern),
+                              (args.g.n_chunks + kPipeTileChunks - 1) / kPipeTileChunks, s, kPipeSmem);
+    kern<<<grid, kThreads, kPipeSmem, s>>>(args, 0.0f);
+    return launch_status();
+  }
   const int64_t per_cta = static_cast<int64_t>(kThreads) * kUnroll;
   const int64_t work = (args.g.n_chunks + per_cta - 1) / per_cta;
   if (args.g.vec) return go(&quant8_kernel<FMT, DT, MODE, STATS, true>, args, work, s);
