@@ -152,6 +152,95 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# Every format of the five named workloads (workload 5: its first 4096 rows, 268 MB, to
+# bound the input generation time), timed per call: quantize with the fused error stats
+# (including the in-library amax pass where the scale is per tensor) and dequantize.
+MATRIX = [
+    (1, None, [("int8", "tensor"), ("e4m3", "tensor"), ("mxfp4", "block"), ("nvfp4", "block")]),
+    (2, None, [("int8", "row"), ("e4m3", "row"), ("mxfp4", "block"), ("nvfp4", "block")]),
+    (3, None, [("e4m3", "row"), ("e5m2", "row"), ("nvfp4", "block")]),
+    (4, None, [("mxfp4", "block"), ("nvfp4", "block")]),
+    (5, 4096, [(f, g) for f in ("int8", "e4m3", "e5m2") for g in ("unit", "tensor")] +
+              [(f, g) for f in ("mxfp4", "nvfp4") for g in ("unit", "block")]),
+]
+
+
+def measure_matrix(dev, peaks, flush, x4=None, reps=10, which=(1, 2, 3, 4, 5)) -> list:
+    import numpy as np
+    import torch
+    import precision_quantization_gb300 as qz
+    import workloads as W
+    out = []
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    ws = qz.Workspace(dev)
+    st = torch.empty((qz.STATS_BYTES,), dtype=torch.uint8, device=dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    for k, rows, runs in MATRIX:
+        if k not in which:
+            continue
+        if k == 4 and x4 is not None:
+            x_np, x = None, x4
+        else:
+            x_np = W.workload(k, rows=rows)
+            if x_np.dtype == np.uint16:
+                x = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16).to(dev)
+            else:
+                x = torch.from_numpy(x_np).to(dev)
+        r, c = x.shape
+        n = r * c
+        eb = x.element_size()
+        idt = qz.QZ_BF16 if x.dtype == torch.bfloat16 else qz.QZ_F32
+        name = W.WORKLOADS[k]["name"] + ("" if rows is None else f" (first {rows} rows)")
+        for fname, gname in runs:
+            f, g = qz.FORMATS[fname], qz.GRANULARITIES[gname]
+            codes, scales, ts = qz.alloc_outputs(f, g, r, c, dev)
+            y = torch.empty((r, c), dtype=x.dtype, device=dev)
+            d = qz.make_desc(f, idt, g, r, c)
+            amax_pass = g == qz.QZ_GRAN_TENSOR or (f == qz.QZ_NVFP4 and g == qz.QZ_GRAN_BLOCK)
+
+            def q():
+                rc = qz.qz_quantize(d, x.data_ptr(), codes.data_ptr(), qz._ptr(scales), ts.data_ptr(),
+                                    None, st.data_ptr(), ws.ptr, sp)
+                assert rc == 0, rc
+
+            def dq():
+                rc = qz.qz_dequantize(d, codes.data_ptr(), qz._ptr(scales), ts.data_ptr(),
+                                      y.data_ptr(), idt, sp)
+                assert rc == 0, rc
+            qms, dms = timed(q), timed(dq)
+            cb = codes.numel() + (0 if scales is None else scales.numel() * scales.element_size()) + 4
+            qb = n * eb * (2 if amax_pass else 1) + cb + 32
+            db = cb + n * eb
+            out.append({"workload": name, "format": fname, "granularity": gname,
+                        "quantize_us": round(qms * 1e3, 1),
+                        "quantize_gbs": round(qb / qms / 1e6, 1),
+                        "quantize_frac": round(qb / qms / 1e6 / peaks["hbm_gbs"], 3),
+                        "quantize_launches": 2 if amax_pass else 1,
+                        "dequantize_us": round(dms * 1e3, 1),
+                        "dequantize_gbs": round(db / dms / 1e6, 1),
+                        "dequantize_frac": round(db / dms / 1e6 / peaks["hbm_gbs"], 3)})
+        del x
+    if ws.status() != 0:
+        raise RuntimeError("status flags set during the format matrix")
+    return out
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -258,6 +347,12 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-matrix", action="store_true",
+                    help="skip the per-format matrix over the five workloads")
+    ap.add_argument("--matrix-only", action="store_true",
+                    help="print only the per-format matrix (one JSON line)")
+    ap.add_argument("--matrix-workloads", default="1,2,3,4,5",
+                    help="comma-separated workload numbers of the matrix")
     ap.add_argument("--rows", type=int, default=ROWS,
                     help="rows of the workload (same recipe); the default is the full size")
     args = ap.parse_args()
@@ -275,6 +370,12 @@ def main():
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    which = tuple(int(v) for v in args.matrix_workloads.split(",") if v)
+    if args.matrix_only:
+        flush = torch.empty((L2_FLUSH_BYTES,), dtype=torch.uint8, device=dev)
+        m = measure_matrix(dev, measured_peaks(), flush, which=which)
+        print(json.dumps({"metric": METRIC, "unit": "GB/s", "formats": m}), flush=True)
+        return
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
@@ -398,6 +499,10 @@ def main():
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": round(em, 3)}
 
+    matrix = None
+    if not args.no_matrix and rank == 0:
+        matrix = measure_matrix(dev, measured_peaks(), flush, x4=x if rows == ROWS else None,
+                                which=which)
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
@@ -437,6 +542,7 @@ def main():
                       "mse": stats_host[qz.QZ_NVFP4].mse,
                       "max_rel_err": stats_host[qz.QZ_NVFP4].max_rel_err},
         },
+        "formats": matrix,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps * len(names),
