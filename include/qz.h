@@ -52,9 +52,11 @@
  * Blocks run along cols.  MXFP4 needs cols % 32 == 0, NVFP4 cols % 16 == 0.
  *
  * Ownership and concurrency.  The caller allocates every buffer (all device memory except
- * the host pointer of qz_get_device_status).  The library allocates nothing and keeps no
- * global state.  Every call is asynchronous on `stream` (NULL = the legacy default
- * stream); argument errors are returned synchronously, before anything is enqueued.
+ * the host pointer of qz_get_device_status).  The library allocates nothing; its only
+ * host-side state is a per-device cache of launch parameters (SM count, resident CTAs per
+ * SM, shared-memory opt-ins), guarded by a mutex.  Every call is asynchronous on `stream`
+ * (NULL = the legacy default stream); argument errors are returned synchronously, before
+ * anything is enqueued.
  * Calls that share one workspace must be ordered on one stream.
  *
  * Alignment.  Pointers need only the natural alignment of their element type.  Fast

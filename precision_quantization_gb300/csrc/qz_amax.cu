@@ -158,8 +158,7 @@ qz_status run(const qz_desc& d, const void* x, float* out, void* ws, cudaStream_
   const Geom g = make_geom(d, x, Elem<DT>::kBytes, 32);
   if (g.vec && g.dense) {
     auto kern = &amax_pipe_kernel<DT>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kPipeSmem)) != cudaSuccess)
+    if (!set_dyn_smem(reinterpret_cast<const void*>(kern), static_cast<int>(kPipeSmem)))
       return QZ_ERR_CUDA;
     const int grid = grid_for(reinterpret_cast<const void*>(kern),
                               (g.n_chunks + kPipeTileChunks - 1) / kPipeTileChunks, s, kPipeSmem);

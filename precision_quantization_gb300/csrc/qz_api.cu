@@ -2,6 +2,7 @@
 // validation on the host, then the kernel launches on the caller's stream.
 #include <climits>
 #include <cstdint>
+#include <mutex>
 
 #include "qz_device.cuh"
 #include "qz_internal.h"
@@ -24,17 +25,81 @@ Geom make_geom(const qz_desc& d, const void* hp, int eb, int align) {
   return g;
 }
 
+// Launch parameters that depend only on the kernel and the device (SM count, resident CTAs
+// per SM, the dynamic shared-memory opt-in), looked up once and reused: a call then costs
+// the launch alone, not a round of driver queries.
+namespace {
+constexpr int kCacheDevices = 64;
+constexpr int kCacheSlots = 1024;
+struct LaunchEntry {
+  const void* kernel;
+  size_t smem;
+  int dev;
+  int occ;
+};
+std::mutex g_launch_mu;
+LaunchEntry g_launch[kCacheSlots];
+int g_launch_n = 0;
+int g_sms[kCacheDevices];
+}  // namespace
+
 int grid_for(const void* kernel, int64_t work_ctas, cudaStream_t, size_t dyn_smem) {
   int dev = 0, sms = 1, occ = 1;
   cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, dyn_smem);
+  bool cached = false;
+  {
+    std::lock_guard<std::mutex> lock(g_launch_mu);
+    if (dev >= 0 && dev < kCacheDevices && g_sms[dev] > 0) {
+      sms = g_sms[dev];
+      for (int i = 0; i < g_launch_n; ++i)
+        if (g_launch[i].kernel == kernel && g_launch[i].smem == dyn_smem && g_launch[i].dev == dev) {
+          occ = g_launch[i].occ;
+          cached = true;
+          break;
+        }
+    }
+  }
+  if (!cached) {
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, dyn_smem);
+    std::lock_guard<std::mutex> lock(g_launch_mu);
+    if (dev >= 0 && dev < kCacheDevices) {
+      g_sms[dev] = sms;
+      if (g_launch_n < kCacheSlots && occ > 0) g_launch[g_launch_n++] = LaunchEntry{kernel, dyn_smem, dev, occ};
+    }
+  }
   if (occ < 1) occ = 1;
   int64_t g = static_cast<int64_t>(sms) * occ;
   if (work_ctas < g) g = work_ctas;
   if (g < 1) g = 1;
   if (g > kMaxCtas) g = kMaxCtas;
   return static_cast<int>(g);
+}
+
+namespace {
+struct AttrEntry {
+  const void* kernel;
+  int dev;
+  int bytes;
+};
+std::mutex g_attr_mu;
+AttrEntry g_attr[kCacheSlots];
+int g_attr_n = 0;
+}  // namespace
+
+bool set_dyn_smem(const void* kernel, int bytes) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  {
+    std::lock_guard<std::mutex> lock(g_attr_mu);
+    for (int i = 0; i < g_attr_n; ++i)
+      if (g_attr[i].kernel == kernel && g_attr[i].dev == dev && g_attr[i].bytes >= bytes) return true;
+  }
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return false;
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  if (g_attr_n < kCacheSlots) g_attr[g_attr_n++] = AttrEntry{kernel, dev, bytes};
+  return true;
 }
 
 namespace {

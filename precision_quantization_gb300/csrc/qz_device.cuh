@@ -155,10 +155,13 @@ __device__ __forceinline__ float div_by(float x, float s, float r) {
 }
 
 // Range in which div_by is exact for every quotient that can change a code: s in
-// [2^-80, 2^100] keeps 1/s normal and every x whose quotient reaches the first rounding
-// threshold of any element format (>= 2^-18) at |x| >= 2^-98, far from underflow.
+// [2^-80, 2^126] keeps 1/s a normal number, and every x whose quotient reaches the first
+// rounding threshold of any element format (>= 2^-18) has |x| >= 2^-98, far from
+// underflow.  Every scale computed from a finite amax lies below 2^126 (INT8 <= 2^121,
+// NVFP4 <= 2^125.4).  The quotients themselves must stay below 2^126 (callers check the
+// block / chunk amax times 1/s where a supplied amax could make them larger).
 __device__ __forceinline__ bool fast_div_ok(float s) {
-  return s >= 0x1p-80f && s <= 0x1p100f;
+  return s >= 0x1p-80f && s <= 0x1p126f;
 }
 
 // ---------------------------------------------------------------------------------------
@@ -309,19 +312,29 @@ __device__ __forceinline__ uint32_t nv_block_code(float t, int scale_round) {
 // rare candidates get an exact __fdiv_rn.  No ratio exceeds 1 (0 is a grid value, so the
 // nearest code is never farther from x than 0 is), so once T == 1 the test is skipped.
 struct StatAcc {
-  float s = 0.0f, c = 0.0f;  // chunks whose errors lie in [2^-40, 2^40]
-  double d = 0.0;            // other chunks (sums that fp32 would over- or underflow)
+  // sum of e^2 in three fixed-scale compensated fp32 buckets, chosen by the largest |e| of
+  // a chunk: [2^-40, 2^40] unscaled; above 2^40 scaled by 2^-90; below 2^-40 by 2^+87.
+  // Each bucket's squares stay inside the normal fp32 range (no overflow, no flush), so
+  // no fp64 arithmetic is needed per chunk.
+  float s = 0.0f, c = 0.0f;
+  float sL = 0.0f, cL = 0.0f;
+  float sS = 0.0f, cS = 0.0f;
+  double d = 0.0;  // chunks accumulated in fp64 by the older element-wise kernels
   float max_abs = 0.0f;
   float rel = 0.0f;   // this lane's exact best ratio
   float T = 0.0f;     // warp-uniform: max of `rel` over the warp
 };
 
-__device__ __forceinline__ void acc_add_sum(StatAcc& a, float p) {
-  const float hi = fmaxf(a.s, p), lo = fminf(a.s, p);
+// Fast2Sum of p into the compensated pair (s, c), larger operand first
+__device__ __forceinline__ void comp_add(float& s, float& c, float p) {
+  const float hi = fmaxf(s, p), lo = fminf(s, p);
   const float t = __fadd_rn(hi, lo);
-  a.c = __fadd_rn(a.c, __fsub_rn(lo, __fsub_rn(t, hi)));
-  a.s = t;
+  c = __fadd_rn(c, __fsub_rn(lo, __fsub_rn(t, hi)));
+  s = t;
 }
+__device__ __forceinline__ void acc_add_sum(StatAcc& a, float p) { comp_add(a.s, a.c, p); }
+constexpr float kLargeScale = 0x1p-90f;  // squares weigh 2^180
+constexpr float kSmallScale = 0x1p87f;   // squares weigh 2^-174
 
 // Is element (x, e) a candidate for a new maximum ratio?
 __device__ __forceinline__ bool rel_candidate(float T, float x, float ae) {
@@ -390,7 +403,13 @@ __device__ __forceinline__ void stats_finish(const StatAcc& a, void* ws, qz_stat
   __shared__ float s_abs[kWarps], s_rel[kWarps];
   __shared__ bool s_last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  double sum = warp_sum(static_cast<double>(a.s) + static_cast<double>(a.c) + a.d);
+  // a bucket whose sum reached +Inf (x^ beyond the fp32 range) has a NaN compensation
+  // term (Inf - Inf); the sum alone is then the answer
+  const auto bucket = [](float s, float c) {
+    return static_cast<double>(s) + (isinf(s) ? 0.0 : static_cast<double>(c));
+  };
+  double sum = warp_sum(bucket(a.s, a.c) + a.d + ldexp(bucket(a.sL, a.cL), 180) +
+                        ldexp(bucket(a.sS, a.cS), -174));
   float mabs = warp_max(a.max_abs), mrel = warp_max(a.rel);
   if (lane == 0) {
     s_sum[warp] = sum;

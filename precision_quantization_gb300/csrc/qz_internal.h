@@ -24,6 +24,9 @@ Geom make_geom(const qz_desc& d, const void* hp, int elem_bytes, int align_bytes
 // the partial-result slots of the workspace.
 int grid_for(const void* kernel, int64_t work_ctas, cudaStream_t stream, size_t dyn_smem = 0);
 
+// Opt `kernel` in to `bytes` of dynamic shared memory on the current device (once).
+bool set_dyn_smem(const void* kernel, int bytes);
+
 qz_status launch_amax(const qz_desc& d, const void* x, float* out, void* ws, cudaStream_t s);
 
 qz_status launch_quant8(const qz_desc& d, const void* x, void* codes, void* scales,

@@ -128,20 +128,21 @@ struct Pairs {
   uint64_t v[NP];
 };
 
-// Sum of squares of 2*NP errors in fp64 -- only for chunks whose largest |e| lies outside
-// [2^-40, 2^40], where fp32 squares could overflow or flush to zero.  Out of line, so the
-// common path carries none of its instructions.
+// Sum of the squares of 2*NP values held as fp32 pairs (two accumulator chains)
 template <int NP>
-__device__ __noinline__ double pairs_sumsq_f64(Pairs<NP> e) {
-  double d = 0.0;
+__device__ __forceinline__ float pairs_sumsq(const uint64_t (&e)[NP]) {
+  uint64_t pa = mul2(e[0], e[0]);
+  uint64_t pb = pk(0.0f, 0.0f);
+  if constexpr (NP > 1) pb = mul2(e[1], e[1]);
 #pragma unroll
-  for (int p = 0; p < NP; ++p) {
-    float e0, e1;
-    upk(e.v[p], e0, e1);
-    d = fma(static_cast<double>(e0), static_cast<double>(e0), d);
-    d = fma(static_cast<double>(e1), static_cast<double>(e1), d);
+  for (int p = 2; p < NP; p += 2) {
+    pa = fma2(e[p], e[p], pa);
+    if (p + 1 < NP) pb = fma2(e[p + 1], e[p + 1], pb);
   }
-  return d;
+  float p0, p1, p2, p3;
+  upk(pa, p0, p1);
+  upk(pb, p2, p3);
+  return __fadd_rn(__fadd_rn(p0, p1), __fadd_rn(p2, p3));
 }
 
 // Largest |value| of 2*NP values held as fp32 pairs: a tree of 3-input maxima.
@@ -177,19 +178,17 @@ __device__ __forceinline__ void acc_pairs(StatAcc& acc, const uint64_t (&xp)[NP]
   if (cm <= 0x1p40f && (cm >= 0x1p-40f || cm == 0.0f)) {
     // every e^2 <= 2^80 and the chunk sum >= 2^-80: no overflow, and the squares that
     // underflow (|e| < 2^-75) are below 2^-70 of the chunk's largest
-    uint64_t pa = mul2(e.v[0], e.v[0]);
-    uint64_t pb = NP > 1 ? mul2(e.v[NP > 1 ? 1 : 0], e.v[NP > 1 ? 1 : 0]) : pk(0.0f, 0.0f);
-#pragma unroll
-    for (int p = 2; p < NP; p += 2) {
-      pa = fma2(e.v[p], e.v[p], pa);
-      if (p + 1 < NP) pb = fma2(e.v[p + 1], e.v[p + 1], pb);
-    }
-    float p0, p1, p2, p3;
-    upk(pa, p0, p1);
-    upk(pb, p2, p3);
-    tpart = __fadd_rn(tpart, __fadd_rn(__fadd_rn(p0, p1), __fadd_rn(p2, p3)));
+    tpart = __fadd_rn(tpart, pairs_sumsq<NP>(e.v));
   } else {
-    acc.d += pairs_sumsq_f64<NP>(e);
+    // outside [2^-40, 2^40]: squares of the power-of-two-scaled errors (exact scaling)
+    const float sc = cm > 0x1p40f ? kLargeScale : kSmallScale;
+    const uint64_t sc2 = pk(sc, sc);
+    uint64_t es[NP];
+#pragma unroll
+    for (int p = 0; p < NP; ++p) es[p] = mul2(e.v[p], sc2);
+    const float part = pairs_sumsq<NP>(es);
+    if (cm > 0x1p40f) comp_add(acc.sL, acc.cL, part);
+    else comp_add(acc.sS, acc.cS, part);
   }
   if constexpr (REL) {  // see rel_candidate
     bool cand = false;

@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kThreads) quant4_kernel(Q4Args a) {
           for (int i = 0; i < EPC; ++i) v[i] = copysignf(0.0f, xs[i]);
         } else {
           const float r = __frcp_rn(s);
-          if (fast_div_ok(s) && __fmul_rn(A, r) <= 0x1p100f) {
+          if (fast_div_ok(s) && __fmul_rn(A, r) <= 0x1p126f) {
 #pragma unroll
             for (int i = 0; i < EPC; ++i) v[i] = div_by(xs[i], s, r);
           } else {
@@ -202,27 +202,6 @@ constexpr int kCPT = kPipeCPT;
 constexpr int kTileChunks = kPipeTileChunks;
 constexpr int kTileBytes = kPipeTileBytes;
 constexpr int kStages = kPipeStages;
-
-template <int NP>
-struct PairsF32 {
-  uint64_t v[NP];
-};
-
-// Sum of squares of one chunk in fp64: only for chunks whose largest |e| lies outside
-// [2^-40, 2^40], where the fp32 squares could overflow or flush to zero.  Kept out of line
-// so the common path carries none of its instructions.
-template <int NP>
-__device__ __noinline__ double sumsq_f64(PairsF32<NP> e) {
-  double d = 0.0;
-#pragma unroll
-  for (int p = 0; p < NP; ++p) {
-    float e0, e1;
-    upk(e.v[p], e0, e1);
-    d = fma(static_cast<double>(e0), static_cast<double>(e0), d);
-    d = fma(static_cast<double>(e1), static_cast<double>(e1), d);
-  }
-  return d;
-}
 
 // Largest magnitude of 2*NP values held as fp32 pairs, as a tree of 3-input maxima (short
 // dependency chains); NAN_PROP selects the NaN-propagating maximum.
@@ -315,7 +294,10 @@ __device__ __forceinline__ void q4_chunk(const Q4Args& a, const Q4Ctx& cx, const
     }
     const float2 sr = cx.tab[scode];
     s = sr.x;
-    if (sr.y != 0.0f && __fmul_rn(A, sr.y) <= 0x1p100f) {
+    if (UNIT) {  // s = 1: fl32(x / 1) = x
+#pragma unroll
+      for (int p = 0; p < NP; ++p) vp[p] = xp[p];
+    } else if (sr.y != 0.0f && __fmul_rn(A, sr.y) <= 0x1p126f) {
       const uint64_t r2 = pk(sr.y, sr.y), ns2 = pk(-s, -s);
 #pragma unroll
       for (int p = 0; p < NP; ++p) vp[p] = div2(xp[p], r2, ns2);
@@ -356,7 +338,7 @@ __device__ __forceinline__ void q4_chunk(const Q4Args& a, const Q4Ctx& cx, const
   if constexpr (!STATS) return;
 
   // x^ = fl32(decode(q) * s), e = fl32(x - x^); lanes without data hold x = 0, q = 0
-  PairsF32<NP> e;
+  Pairs<NP> e;
   if (FMT == QZ_MXFP4 && __all_sync(kFull, mul_exact)) {
     const uint64_t ns2 = pk(-s, -s);
 #pragma unroll
@@ -364,49 +346,9 @@ __device__ __forceinline__ void q4_chunk(const Q4Args& a, const Q4Ctx& cx, const
   } else {
     const uint64_t s2 = pk(s, s), z2 = pk(cx.zero, cx.zero);
 #pragma unroll
-    for (int p = 0; p < NP; ++p)
-      e.v[p] = sub2(xp[p], mul2_rounded(f16x2_to_f32x2(h[p / 4][p % 4]), s2, z2));
+    for (int p = 0; p < NP; ++p) e.v[p] = sub2(xp[p], mul2_rounded(f16x2_to_f32x2(h[p / 4][p % 4]), s2, z2));
   }
-  const float cm = pairs_absmax<NP, false>(e.v);
-  acc.max_abs = fmaxf(acc.max_abs, cm);
-  if (cm <= 0x1p40f && (cm >= 0x1p-40f || cm == 0.0f)) {
-    // every e^2 <= 2^80 and the chunk sum >= 2^-80: no overflow, and the squares that
-    // underflow (|e| < 2^-75) are below 2^-70 of the chunk's largest
-    uint64_t pa = mul2(e.v[0], e.v[0]), pb = mul2(e.v[1], e.v[1]);
-#pragma unroll
-    for (int p = 2; p < NP; p += 2) {
-      pa = fma2(e.v[p], e.v[p], pa);
-      pb = fma2(e.v[p + 1], e.v[p + 1], pb);
-    }
-    float p0, p1, p2, p3;
-    upk(pa, p0, p1);
-    upk(pb, p2, p3);
-    tpart = __fadd_rn(tpart, __fadd_rn(__fadd_rn(p0, p1), __fadd_rn(p2, p3)));
-  } else {
-    acc.d += sumsq_f64<NP>(e);
-  }
-  if constexpr (REL) {  // see rel_candidate
-    bool cand = false;
-#pragma unroll
-    for (int p = 0; p < NP; ++p) {
-      float x0, x1, e0, e1;
-      upk(xp[p], x0, x1);
-      upk(e.v[p], e0, e1);
-      cand |= rel_candidate(acc.T, x0, fabsf(e0)) | rel_candidate(acc.T, x1, fabsf(e1));
-    }
-    if (__any_sync(kFull, cand)) {
-      if (cand) {
-#pragma unroll
-        for (int p = 0; p < NP; ++p) {
-          float x0, x1, e0, e1;
-          upk(xp[p], x0, x1);
-          upk(e.v[p], e0, e1);
-          acc.rel = max3(acc.rel, rel_exact(x0, fabsf(e0)), rel_exact(x1, fabsf(e1)));
-        }
-      }
-      acc.T = warp_max(acc.rel);
-    }
-  }
+  acc_pairs<NP, REL>(acc, xp, e, tpart);
 }
 
 template <int FMT, int DT, bool UNIT, bool STATS, int SR>
@@ -487,8 +429,7 @@ template <int FMT, int DT, bool UNIT, bool STATS>
 qz_status run_pipe(const Q4Args& args, cudaStream_t s) {
   auto kern = args.scale_round == QZ_SCALE_NEAREST ? &quant4_pipe_kernel<FMT, DT, UNIT, STATS, QZ_SCALE_NEAREST>
                                                     : &quant4_pipe_kernel<FMT, DT, UNIT, STATS, QZ_SCALE_UP>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(kPipeSmem)) != cudaSuccess)
+  if (!set_dyn_smem(reinterpret_cast<const void*>(kern), static_cast<int>(kPipeSmem)))
     return QZ_ERR_CUDA;
   const int grid = grid_for(reinterpret_cast<const void*>(kern),
                             (args.g.n_chunks + kTileChunks - 1) / kTileChunks, s, kPipeSmem);

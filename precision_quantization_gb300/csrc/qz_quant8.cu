@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(kThreads) quant8_kernel(Q8Args a) {
 #pragma unroll
         for (int i = 0; i < EPC; ++i) A = absmax_nan(A, chunk_elem<DT>(w[k], i));
         if (valid && !is_finite_f(A)) flag_status(a.ws, QZ_FLAG_NONFINITE_INPUT);
-        if constexpr (MODE == kTensorSupplied) f = f && (__fmul_rn(A, r) <= 0x1p100f);
+        if constexpr (MODE == kTensorSupplied) f = f && (__fmul_rn(A, r) <= 0x1p126f);
       }
       uint8_t* cp = a.codes + row[k] * g.cols + col[k];
       const int64_t nv = g.dense ? EPC : g.cols - col[k];
@@ -329,7 +329,7 @@ __device__ __forceinline__ void q8_chunk(const uint32_t (&w)[8], bool valid, uin
     if constexpr (MODE == kTensorSupplied) {
       float r, rr;
       upk(r2, r, rr);
-      f = f && (__fmul_rn(A, r) <= 0x1p100f);
+      f = f && (__fmul_rn(A, r) <= 0x1p126f);
     }
   }
   uint64_t vp[NP];
@@ -573,8 +573,7 @@ qz_status run_row(const Q8Args& args, cudaStream_t s) {
     auto kern = &quant8_rowpipe_kernel<FMT, DT, STATS>;
     const uint32_t stage = static_cast<uint32_t>((row_bytes + 127) / 128 * 128);
     const size_t smem = 2 * static_cast<size_t>(stage);
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-        cudaSuccess)
+    if (!set_dyn_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem)))
       return QZ_ERR_CUDA;
     const int grid = grid_for(reinterpret_cast<const void*>(kern), rows, s, smem);
     kern<<<grid, kThreads, smem, s>>>(args, 0.0f, stage);
@@ -594,8 +593,7 @@ template <int FMT, int DT, int MODE, bool STATS>
 qz_status run_flat(const Q8Args& args, cudaStream_t s) {
   if (args.g.vec && args.g.dense && reinterpret_cast<uintptr_t>(args.x) % 16 == 0) {
     auto kern = &quant8_pipe_kernel<FMT, DT, MODE, STATS>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kPipeSmem)) != cudaSuccess)
+    if (!set_dyn_smem(reinterpret_cast<const void*>(kern), static_cast<int>(kPipeSmem)))
       return QZ_ERR_CUDA;
     const int grid = grid_for(reinterpret_cast<const void*>(kern),
                               (args.g.n_chunks + kPipeTileChunks - 1) / kPipeTileChunks, s, kPipeSmem);
