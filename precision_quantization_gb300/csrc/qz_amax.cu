@@ -105,22 +105,29 @@ amax_kernel(const void* __restrict__ x, Geom g, float* __restrict__ out, void* w
 
 // Dense tensors: x streamed through shared memory by 1-D bulk copies (16 KiB tiles, four
 // in flight per CTA), so the read runs at the copy engine's pace whatever the occupancy.
+constexpr int kAmaxStages = kPipeStages;
+constexpr int kAmaxCPT = kPipeCPT;
+constexpr int kAmaxTileChunks = kThreads * kAmaxCPT;
+constexpr int kAmaxTileBytes = kAmaxTileChunks * 32;
+constexpr size_t kAmaxSmem = static_cast<size_t>(kAmaxStages) * kAmaxTileBytes;
+
 template <int DT>
 __global__ void __launch_bounds__(kThreads)
 amax_pipe_kernel(const void* __restrict__ x, int64_t n_chunks, float* __restrict__ out, void* ws) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t bars[kPipeStages];
+  __shared__ __align__(8) uint64_t bars[kAmaxStages];
   __shared__ int s_abort;
   const int tid = threadIdx.x;
   if (tid == 0) {
-    for (int i = 0; i < kPipeStages; ++i) mbar_init(smem_addr(&bars[i]), 1);
+    for (int i = 0; i < kAmaxStages; ++i) mbar_init(smem_addr(&bars[i]), 1);
     mbar_init_fence();
     s_abort = 0;
   }
   __syncthreads();
-  BulkPipe<kPipeStages, kPipeTileBytes> P{smem_addr(smem), smem_addr(&bars[0]),
-                                          static_cast<const char*>(x), n_chunks * 32,
-                                          (n_chunks + kPipeTileChunks - 1) / kPipeTileChunks, false};
+  const BulkPipe<kAmaxStages, kAmaxTileBytes> P{smem_addr(smem), smem_addr(&bars[0]),
+                                                static_cast<const char*>(x), n_chunks * 32,
+                                                (n_chunks + kAmaxTileChunks - 1) / kAmaxTileChunks,
+                                                false};
   if (tid == 0) P.prologue();
   uint32_t m = 0;
   for (int64_t k = 0; P.has(k); ++k) {
@@ -128,9 +135,9 @@ amax_pipe_kernel(const void* __restrict__ x, int64_t n_chunks, float* __restrict
     if (!P.wait(k)) s_abort = 1;
     const uint32_t stage = P.stage(k);
 #pragma unroll
-    for (int c = 0; c < kPipeCPT; ++c) {
+    for (int c = 0; c < kAmaxCPT; ++c) {
       const int j = c * kThreads + tid;
-      if (tile * kPipeTileChunks + j < n_chunks) {
+      if (tile * kAmaxTileChunks + j < n_chunks) {
         uint32_t w[8];
         lds32B(w, stage + 32u * j);
 #pragma unroll
@@ -148,7 +155,7 @@ amax_pipe_kernel(const void* __restrict__ x, int64_t n_chunks, float* __restrict
       }
       return;
     }
-    if (tid == 0) P.issue(k + kPipeStages);
+    if (tid == 0) P.issue(k + kAmaxStages);
   }
   amax_finish<DT>(m, out, ws);
 }
@@ -158,11 +165,11 @@ qz_status run(const qz_desc& d, const void* x, float* out, void* ws, cudaStream_
   const Geom g = make_geom(d, x, Elem<DT>::kBytes, 32);
   if (g.vec && g.dense) {
     auto kern = &amax_pipe_kernel<DT>;
-    if (!set_dyn_smem(reinterpret_cast<const void*>(kern), static_cast<int>(kPipeSmem)))
+    if (!set_dyn_smem(reinterpret_cast<const void*>(kern), static_cast<int>(kAmaxSmem)))
       return QZ_ERR_CUDA;
     const int grid = grid_for(reinterpret_cast<const void*>(kern),
-                              (g.n_chunks + kPipeTileChunks - 1) / kPipeTileChunks, s, kPipeSmem);
-    kern<<<grid, kThreads, kPipeSmem, s>>>(x, g.n_chunks, out, ws);
+                              (g.n_chunks + kAmaxTileChunks - 1) / kAmaxTileChunks, s, kAmaxSmem);
+    kern<<<grid, kThreads, kAmaxSmem, s>>>(x, g.n_chunks, out, ws);
     return launch_status();
   }
   if (g.vec) {

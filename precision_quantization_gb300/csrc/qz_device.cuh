@@ -319,8 +319,8 @@ struct StatAcc {
   float s = 0.0f, c = 0.0f;
   float sL = 0.0f, cL = 0.0f;
   float sS = 0.0f, cS = 0.0f;
-  double d = 0.0;  // chunks accumulated in fp64 by the older element-wise kernels
   float max_abs = 0.0f;
+  float max_abs_sq = 0.0f;  // fl32(max_abs^2)
   float rel = 0.0f;   // this lane's exact best ratio
   float T = 0.0f;     // warp-uniform: max of `rel` over the warp
 };
@@ -363,19 +363,20 @@ __device__ __forceinline__ void acc_chunk(StatAcc& acc, const float (&xs)[N], co
     if (want_rel) cand |= rel_candidate(acc.T, xs[i], fabsf(e[i]));
   }
   acc.max_abs = fmaxf(acc.max_abs, cm);
-  if (cm <= 0x1p40f && (cm >= 0x1p-40f || cm == 0.0f)) {
-    // every e^2 <= 2^80 and the chunk sum >= 2^-80: no overflow, and the squares that
-    // underflow (|e| < 2^-75) are below 2^-70 of the chunk's largest
-    float part = 0.0f;
+  // the bucket of the chunk (see StatAcc): scale 1 for a largest |e| in [2^-40, 2^40] (or
+  // 0), where every e^2 <= 2^80 and the squares that underflow (|e| < 2^-75) are below
+  // 2^-70 of the chunk's largest; otherwise the errors scaled by a power of two (exact)
+  const bool normal = cm <= 0x1p40f && (cm >= 0x1p-40f || cm == 0.0f);
+  const float sc = normal ? 1.0f : (cm > 0x1p40f ? kLargeScale : kSmallScale);
+  float part = 0.0f;
 #pragma unroll
-    for (int i = 0; i < N; ++i) part = __fmaf_rn(e[i], e[i], part);
-    acc_add_sum(acc, part);
-  } else {
-    double part = 0.0;
-#pragma unroll
-    for (int i = 0; i < N; ++i) part = fma(static_cast<double>(e[i]), static_cast<double>(e[i]), part);
-    acc.d += part;
+  for (int i = 0; i < N; ++i) {
+    const float es = __fmul_rn(e[i], sc);
+    part = __fmaf_rn(es, es, part);
   }
+  if (normal) comp_add(acc.s, acc.c, part);
+  else if (cm > 0x1p40f) comp_add(acc.sL, acc.cL, part);
+  else comp_add(acc.sS, acc.cS, part);
   if (want_rel && __any_sync(kFull, cand)) {
     if (cand) {
 #pragma unroll
@@ -396,37 +397,67 @@ __device__ __forceinline__ double warp_sum(double v) {
   return v;
 }
 
+// Knuth's TwoSum folded into a compensated pair: (s, c) += (s2, c2), exact error of s + s2
+// kept in c.  Any operand order; an infinite s makes c NaN, which `bucket_value` discards.
+__device__ __forceinline__ void two_sum_into(float& s, float& c, float s2, float c2) {
+  const float t = __fadd_rn(s, s2);
+  const float bb = __fsub_rn(t, s);
+  const float err = __fadd_rn(__fsub_rn(s, __fsub_rn(t, bb)), __fsub_rn(s2, bb));
+  c = __fadd_rn(__fadd_rn(c, c2), err);
+  s = t;
+}
+__device__ __forceinline__ void warp_two_sum(float& s, float& c) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const float s2 = __shfl_xor_sync(kFull, s, o), c2 = __shfl_xor_sync(kFull, c, o);
+    two_sum_into(s, c, s2, c2);
+  }
+}
+// a bucket whose sum reached +Inf (x^ beyond the fp32 range) has a NaN compensation term
+// (Inf - Inf); the sum alone is then the answer
+__device__ __forceinline__ double bucket_value(float s, float c) {
+  return static_cast<double>(s) + (isinf(s) ? 0.0 : static_cast<double>(c));
+}
+
 // CTA reduction of the accumulators into this CTA's partial, then the last CTA to finish
 // (atomicInc wraps the counter back to 0) folds all partials in a fixed order into *out.
+// Within the CTA the three buckets stay compensated fp32 pairs (fp64 arithmetic is slow on
+// this part); one thread per CTA weighs them into the fp64 partial.
 __device__ __forceinline__ void stats_finish(const StatAcc& a, void* ws, qz_stats* out, uint64_t n) {
   __shared__ double s_sum[kWarps];
+  __shared__ float s_b[kWarps][6];
   __shared__ float s_abs[kWarps], s_rel[kWarps];
   __shared__ bool s_last;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  // a bucket whose sum reached +Inf (x^ beyond the fp32 range) has a NaN compensation
-  // term (Inf - Inf); the sum alone is then the answer
-  const auto bucket = [](float s, float c) {
-    return static_cast<double>(s) + (isinf(s) ? 0.0 : static_cast<double>(c));
-  };
-  double sum = warp_sum(bucket(a.s, a.c) + a.d + ldexp(bucket(a.sL, a.cL), 180) +
-                        ldexp(bucket(a.sS, a.cS), -174));
+  float b[6] = {a.s, a.c, a.sL, a.cL, a.sS, a.cS};
+#pragma unroll
+  for (int k = 0; k < 3; ++k) warp_two_sum(b[2 * k], b[2 * k + 1]);
   float mabs = warp_max(a.max_abs), mrel = warp_max(a.rel);
   if (lane == 0) {
-    s_sum[warp] = sum;
+#pragma unroll
+    for (int k = 0; k < 6; ++k) s_b[warp][k] = b[k];
     s_abs[warp] = mabs;
     s_rel[warp] = mrel;
   }
   __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int k = 0; k < 6; ++k) b[k] = lane < kWarps ? s_b[lane][k] : 0.0f;
+#pragma unroll
+    for (int k = 0; k < 3; ++k) warp_two_sum(b[2 * k], b[2 * k + 1]);
+    if (lane == 0)
+      s_sum[0] = bucket_value(b[0], b[1]) + ldexp(bucket_value(b[2], b[3]), 180) +
+                 ldexp(bucket_value(b[4], b[5]), -174);
+  }
+  __syncthreads();
   StatPartial* parts = ws_stat_partials(ws);
   if (threadIdx.x == 0) {
-    double t = 0.0;
     float ma = 0.0f, mr = 0.0f;
     for (int w = 0; w < kWarps; ++w) {
-      t += s_sum[w];
       ma = fmaxf(ma, s_abs[w]);
       mr = fmaxf(mr, s_rel[w]);
     }
-    parts[blockIdx.x].sum_sq = t;
+    parts[blockIdx.x].sum_sq = s_sum[0];
     parts[blockIdx.x].max_abs = ma;
     parts[blockIdx.x].max_rel = mr;
     __threadfence();

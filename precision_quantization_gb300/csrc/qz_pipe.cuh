@@ -71,9 +71,15 @@ __device__ __forceinline__ float max3(float m, float a, float b) {
   return d;
 }
 
-// two bf16 in one word -> fp32 pair {lo, hi}
+// two bf16 in one word -> fp32 pair {lo, hi}: x + (-0) with a bf16 operand widens it
+// exactly (signed zeros and subnormals kept) on the FMA pipe instead of the integer ALU
 __device__ __forceinline__ uint64_t widen_bf16x2(uint32_t w) {
-  return pk(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  float lo, hi;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "add.rn.f32.bf16 %0, l, %3;\n\tadd.rn.f32.bf16 %1, h, %3;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(w), "f"(-0.0f));
+  return pk(lo, hi);
 }
 
 // Eight quotients -> one 32-bit word of E2M1 codes (element 0 in bits [0,4)) and the
@@ -115,6 +121,23 @@ __device__ __forceinline__ uint64_t f16x2_to_f32x2(uint32_t h) {
       : "=l"(r)
       : "r"(h));
   return r;
+}
+
+// e = fl32(x - q * 2^k) for the two code values q of the f16x2 word h, given -2^k as the
+// f16 bits ns16 (k in [-24, 15]): one fused multiply-add per element whose f16 operands
+// widen exactly, so each result is rounded once
+__device__ __forceinline__ uint64_t fma_f16_pair(uint32_t h, uint16_t ns16, uint64_t x) {
+  float x0, x1, e0, e1;
+  upk(x, x0, x1);
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "fma.rn.f32.f16 %0, l, %3, %4;\n\tfma.rn.f32.f16 %1, h, %3, %5;\n\t}"
+      : "=f"(e0), "=f"(e1)
+      : "r"(h), "h"(ns16), "f"(x0), "f"(x1));
+  return pk(e0, e1);
+}
+// f16 bits of -2^k, k in [-24, 15] (k < -14: an f16 subnormal)
+__device__ __forceinline__ uint16_t f16_neg_pow2(int k) {
+  return static_cast<uint16_t>(0x8000u | (k >= -14 ? static_cast<uint32_t>(k + 15) << 10 : 1u << (k + 24)));
 }
 
 __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
@@ -166,29 +189,43 @@ __device__ __forceinline__ float pairs_max_abs(const uint64_t (&p2)[NP]) {
   return m;
 }
 
-// Accumulate the errors e (fp32 pairs) of one chunk whose inputs are x: largest |e| and
-// sum of e^2 (into tpart when every |e| lies in [2^-40, 2^40], else in fp64), and -- REL,
-// while the warp's exact max |e|/|x| search is open -- the candidates of rel_candidate.
-// Every lane of the warp must make the same calls (the REL part votes).
+// Accumulate the errors e (fp32 pairs) of one chunk whose inputs are x: largest |e|, sum
+// of e^2, and -- REL, while the warp's exact max |e|/|x| search is open -- the candidates
+// of rel_candidate.  Every lane of the warp must make the same calls (the REL part votes).
+//
+// Largest |e|: the chunk's fp32 sum of squares `part` is at least fl(e^2) of each of its
+// elements (RN is monotone and never rounds a sum of non-negative terms below a term), so
+// part < fl(max_abs^2) proves every |e| < max_abs and the chunk is skipped.
+// Sum of squares: `part` itself when it lies in [2^-80, 2^80] (no square overflowed, and
+// the squares below the normal range are under 2^-42 of the chunk's largest); otherwise
+// the chunk's errors go, scaled by a power of two (exact), to the bucket of their largest
+// magnitude (see StatAcc).
 template <int NP, bool REL>
 __device__ __forceinline__ void acc_pairs(StatAcc& acc, const uint64_t (&xp)[NP], const Pairs<NP>& e,
                                           float& tpart) {
-  const float cm = pairs_max_abs<NP>(e.v);
-  acc.max_abs = fmaxf(acc.max_abs, cm);
-  if (cm <= 0x1p40f && (cm >= 0x1p-40f || cm == 0.0f)) {
-    // every e^2 <= 2^80 and the chunk sum >= 2^-80: no overflow, and the squares that
-    // underflow (|e| < 2^-75) are below 2^-70 of the chunk's largest
-    tpart = __fadd_rn(tpart, pairs_sumsq<NP>(e.v));
+  const float part = pairs_sumsq<NP>(e.v);
+  float cm = -1.0f;  // largest |e| of the chunk, -1 while not needed
+  if (!(part < acc.max_abs_sq)) {
+    cm = pairs_max_abs<NP>(e.v);
+    acc.max_abs = fmaxf(acc.max_abs, cm);
+    acc.max_abs_sq = __fmul_rn(acc.max_abs, acc.max_abs);
+  }
+  if (part >= 0x1p-80f && part <= 0x1p80f) {
+    tpart = __fadd_rn(tpart, part);
   } else {
-    // outside [2^-40, 2^40]: squares of the power-of-two-scaled errors (exact scaling)
-    const float sc = cm > 0x1p40f ? kLargeScale : kSmallScale;
-    const uint64_t sc2 = pk(sc, sc);
-    uint64_t es[NP];
+    if (cm < 0.0f) cm = pairs_max_abs<NP>(e.v);
+    if (cm <= 0x1p40f && (cm >= 0x1p-40f || cm == 0.0f)) {
+      tpart = __fadd_rn(tpart, part);
+    } else {
+      const float sc = cm > 0x1p40f ? kLargeScale : kSmallScale;
+      const uint64_t sc2 = pk(sc, sc);
+      uint64_t es[NP];
 #pragma unroll
-    for (int p = 0; p < NP; ++p) es[p] = mul2(e.v[p], sc2);
-    const float part = pairs_sumsq<NP>(es);
-    if (cm > 0x1p40f) comp_add(acc.sL, acc.cL, part);
-    else comp_add(acc.sS, acc.cS, part);
+      for (int p = 0; p < NP; ++p) es[p] = mul2(e.v[p], sc2);
+      const float ps = pairs_sumsq<NP>(es);
+      if (cm > 0x1p40f) comp_add(acc.sL, acc.cL, ps);
+      else comp_add(acc.sS, acc.cS, ps);
+    }
   }
   if constexpr (REL) {  // see rel_candidate
     bool cand = false;
@@ -282,7 +319,8 @@ constexpr size_t kPipeSmem = static_cast<size_t>(kPipeStages) * kPipeTileBytes;
 // Streams the tiles of one CTA through S shared-memory stages.  Tile k of this CTA is
 // tile (blockIdx.x + k * gridDim.x) of the tensor (counted from the end when `reverse`),
 // TILE bytes (the last tile of the tensor shorter).
-// Thread 0 issues the copies; every thread waits on the tile's barrier.
+// Thread 0 issues the copies; every thread waits on the tile's barrier; the CTA
+// synchronises once per tile before thread 0 refills the stage it has left.
 template <int S, int TILE>
 struct BulkPipe {
   uint32_t base;      // shared address of stage 0
@@ -328,7 +366,7 @@ struct BulkPipe {
   __device__ __forceinline__ void drain(int64_t k) const {
     for (int64_t j = k; j < k + S; ++j)
       if (has(j)) mbar_wait(bars + 8u * static_cast<uint32_t>(j % S),
-                                         static_cast<uint32_t>((j / S) & 1), kWaitLimitNs);
+                            static_cast<uint32_t>((j / S) & 1), kWaitLimitNs);
   }
 };
 

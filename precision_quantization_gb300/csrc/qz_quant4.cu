@@ -269,8 +269,9 @@ __device__ __forceinline__ void q4_chunk(const Q4Args& a, const Q4Ctx& cx, const
   float s;
   uint64_t vp[NP];
   bool mul_exact = false;  // MXFP4: decode(q) * 2^k exact, so e = fma(-q, s, x)
+  int kexp = 0;
   if constexpr (FMT == QZ_MXFP4) {
-    const int kexp = UNIT ? 0 : mx_exponent(div6(A), SR);
+    kexp = UNIT ? 0 : mx_exponent(div6(A), SR);
     scode = static_cast<uint32_t>(kexp + 127);
     s = exp2_pos(kexp);
     const float inv = exp2_neg(kexp);
@@ -339,7 +340,11 @@ __device__ __forceinline__ void q4_chunk(const Q4Args& a, const Q4Ctx& cx, const
 
   // x^ = fl32(decode(q) * s), e = fl32(x - x^); lanes without data hold x = 0, q = 0
   Pairs<NP> e;
-  if (FMT == QZ_MXFP4 && __all_sync(kFull, mul_exact)) {
+  if (FMT == QZ_MXFP4 && __all_sync(kFull, kexp >= -24 && kexp <= 15)) {
+    const uint16_t ns16 = f16_neg_pow2(kexp);  // -s exactly, as an f16 operand
+#pragma unroll
+    for (int p = 0; p < NP; ++p) e.v[p] = fma_f16_pair(h[p / 4][p % 4], ns16, xp[p]);
+  } else if (FMT == QZ_MXFP4 && __all_sync(kFull, mul_exact)) {
     const uint64_t ns2 = pk(-s, -s);
 #pragma unroll
     for (int p = 0; p < NP; ++p) e.v[p] = fma2(f16x2_to_f32x2(h[p / 4][p % 4]), ns2, xp[p]);
@@ -383,9 +388,9 @@ __global__ void __launch_bounds__(kThreads, 3) quant4_pipe_kernel(Q4Args a) {
     s_abort = 0;
   }
   __syncthreads();
-  BulkPipe<kStages, kTileBytes> P{smem_addr(smem), smem_addr(&bars[0]),
-                                  static_cast<const char*>(a.x), n_chunks * 32,
-                                  (n_chunks + kTileChunks - 1) / kTileChunks, a.reverse};
+  const BulkPipe<kStages, kTileBytes> P{smem_addr(smem), smem_addr(&bars[0]),
+                                        static_cast<const char*>(a.x), n_chunks * 32,
+                                        (n_chunks + kTileChunks - 1) / kTileChunks, a.reverse};
   if (tid == 0) P.prologue();
 
   StatAcc acc;

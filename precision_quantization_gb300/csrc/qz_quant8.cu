@@ -400,9 +400,10 @@ __global__ void __launch_bounds__(kThreads, 3) quant8_pipe_kernel(Q8Args a, floa
     s_abort = 0;
   }
   __syncthreads();
-  BulkPipe<kPipeStages, kPipeTileBytes> P{smem_addr(smem), smem_addr(&bars[0]),
-                                          static_cast<const char*>(a.x), n_chunks * 32,
-                                          (n_chunks + kPipeTileChunks - 1) / kPipeTileChunks, false};
+  const BulkPipe<kPipeStages, kPipeTileBytes> P{smem_addr(smem), smem_addr(&bars[0]),
+                                                static_cast<const char*>(a.x), n_chunks * 32,
+                                                (n_chunks + kPipeTileChunks - 1) / kPipeTileChunks,
+                                                false};
   if (tid == 0) P.prologue();
   StatAcc acc;
   for (int64_t k = 0; P.has(k); ++k) {
