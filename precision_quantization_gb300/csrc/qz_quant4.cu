@@ -271,7 +271,19 @@ __device__ __forceinline__ void q4_chunk(const Q4Args& a, const Q4Ctx& cx, const
   bool mul_exact = false;  // MXFP4: decode(q) * 2^k exact, so e = fma(-q, s, x)
   int kexp = 0;
   if constexpr (FMT == QZ_MXFP4) {
-    kexp = UNIT ? 0 : mx_exponent(div6(A), SR);
+    if constexpr (UNIT) {
+      kexp = 0;
+    } else if constexpr (SR == QZ_SCALE_UP) {
+      // With A = m * 2^e (m in [1,2)), A/6 = (m/1.5) * 2^(e-2): fl32(A/6) <= 2^(e-2) exactly
+      // when m <= 1.5, and lies in (2^(e-2), 2^(e-1)) otherwise, so the smallest k with
+      // 2^k >= fl32(A/6) is e - 2 + [m > 1.5] -- read off A's fields, valid while A/6 is
+      // normal (A >= 2^-123).  A = 0 gives -129, clamped to -127.
+      const uint32_t b = __float_as_uint(A);
+      kexp = max(-127, static_cast<int>(b >> 23) - 129 + ((b & 0x7fffffu) > 0x400000u ? 1 : 0));
+      if (b - 1u < 0x01ffffffu || b >= 0x7f800000u) kexp = mx_exponent(div6(A), SR);
+    } else {
+      kexp = mx_exponent(div6(A), SR);
+    }
     scode = static_cast<uint32_t>(kexp + 127);
     s = exp2_pos(kexp);
     const float inv = exp2_neg(kexp);

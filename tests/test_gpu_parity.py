@@ -124,6 +124,24 @@ def test_tiny_and_huge_tensors(fmt, gran):
         assert_parity(run_gpu(x, fmt, gran), run_oracle(x, fmt, gran))
 
 
+@pytest.mark.parametrize("scale_round", [O.SCALE_UP, O.SCALE_NEAREST])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("fmt", FMT4)
+def test_rows_of_mixed_magnitude(fmt, dtype, scale_round):
+    """Rows scaled by 10^u, u uniform in [-35, 32]: the chunks' squared errors leave the
+    plain fp32 range in some rows and not in others (range buckets of the fused sum), and
+    the MXFP4 exponent comes from both the amax-field rule and the division route."""
+    rng = np.random.default_rng(610)
+    x = W.lognormal_signed(96, 4096, seed=611, sigma=2.0, dtype="f32")
+    x = (x * (10.0 ** rng.uniform(-35, 32, size=(96, 1)))).astype(np.float32)
+    x[5] = 0.0
+    x[7, :64] = np.float32(3e-41)
+    if dtype == "bf16":
+        x = W.bf16_bits(x)
+    assert_parity(run_gpu(x, fmt, O.GRAN_BLOCK, scale_round=scale_round),
+                  run_oracle(x, fmt, O.GRAN_BLOCK, scale_round=scale_round))
+
+
 @pytest.mark.parametrize("fmt,gran", [(O.E5M2, O.GRAN_TENSOR), (O.INT8, O.GRAN_ROW),
                                       (O.MXFP4, O.GRAN_BLOCK), (O.NVFP4, O.GRAN_BLOCK)])
 def test_empty(fmt, gran):
