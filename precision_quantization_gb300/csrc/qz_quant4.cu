@@ -240,6 +240,8 @@ struct Q4Ctx {
   bool sg_fast;   // s_global inside the FMA-quotient range
   const float2* tab;
   float zero;     // opaque 0.0f (see mul2_rounded)
+  float c6;       // NVFP4: RN(1 / RN(6 * s_global))
+  bool c6_ok;     // s_global in [2^-100, 2^100]: 6 * s_global and c6 normal
 };
 
 // One 32-byte chunk: block amax, scale, quotients, cast, stores, and (STATS) the error of
@@ -295,13 +297,25 @@ __device__ __forceinline__ void q4_chunk(const Q4Args& a, const Q4Ctx& cx, const
     if constexpr (UNIT) {
       scode = 0x38u;
     } else {
-      const float a6 = div6(A);  // (block_amax / 6) / s_global
-      float t;
-      if (a6 >= 0x1p-100f && cx.sg_fast) {
-        t = div_pos(a6, cx.sg, cx.rg);
-        if (t < 0x1p-120f) t = __fdiv_rn(a6, cx.sg);
-      } else {
-        t = __fdiv_rn(a6, cx.sg);
+      // The ideal scale t = fl32(fl32(A/6) / s_global) decides the block code only through
+      // the E4M3 value (UP) or midpoint (NEAREST) it falls beside.  t' = RN(A * c6) is five
+      // roundings of 2^-24 from t (normal operands: c6_ok, A and t' >= 2^-100, or A = 0),
+      // so t lies within 6 ulp of t'.  E4M3 values have at most 4 significant bits and
+      // their midpoints 5, i.e. fraction fields that are multiples of 2^20 (2^19): when
+      // t' is not within 8 ulp of such a multiple, t and t' get the same code; otherwise
+      // (rare) t is computed as written.
+      float t = __fmul_rn(A, cx.c6);
+      constexpr uint32_t kMask = SR == QZ_SCALE_NEAREST ? 0x7ffffu : 0xfffffu;
+      const uint32_t tb = __float_as_uint(t);
+      const bool near = ((tb + 8u) & kMask) < 16u;
+      if (!cx.c6_ok || near || (A != 0.0f && !(A >= 0x1p-100f && t >= 0x1p-100f))) {
+        const float a6 = div6(A);  // (block_amax / 6) / s_global
+        if (a6 >= 0x1p-100f && cx.sg_fast) {
+          t = div_pos(a6, cx.sg, cx.rg);
+          if (t < 0x1p-120f) t = __fdiv_rn(a6, cx.sg);
+        } else {
+          t = __fdiv_rn(a6, cx.sg);
+        }
       }
       scode = nv_block_code(t, SR);
     }
@@ -377,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 3) quant4_pipe_kernel(Q4Args a) {
   const int tid = threadIdx.x, lane = tid & 31;
   const int64_t n_chunks = a.g.n_chunks;
 
-  Q4Ctx cx{1.0f, 1.0f, true, tab, a.zero};
+  Q4Ctx cx{1.0f, 1.0f, true, tab, a.zero, 0.0f, false};
   if constexpr (FMT == QZ_NVFP4) {
     if constexpr (!UNIT) {
       const float alpha = *a.amax;
@@ -388,6 +402,8 @@ __global__ void __launch_bounds__(kThreads, 3) quant4_pipe_kernel(Q4Args a) {
       cx.rg = __frcp_rn(cx.sg);
     }
     cx.sg_fast = fast_div_ok(cx.sg);
+    cx.c6_ok = cx.sg >= 0x1p-100f && cx.sg <= 0x1p100f;
+    cx.c6 = __frcp_rn(__fmul_rn(6.0f, cx.sg));
     for (int c = tid; c < 128; c += kThreads) {
       const float s = __fmul_rn(cx.sg, dec_e4m3(static_cast<uint32_t>(c)));
       tab[c] = make_float2(s, (s > 0.0f && fast_div_ok(s)) ? __frcp_rn(s) : 0.0f);
