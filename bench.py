@@ -155,13 +155,16 @@ class ClockSampler:
 # Every format of the five named workloads (workload 5: its first 4096 rows, 268 MB, to
 # bound the input generation time), timed per call: quantize with the fused error stats
 # (including the in-library amax pass where the scale is per tensor) and dequantize.
+# "delayed": qz_quantize_delayed, the per-tensor scale from an amax handed in (here the
+# tensor's own, computed beforehand) and this tensor's amax returned, in one pass.
 MATRIX = [
     (1, None, [("int8", "tensor"), ("e4m3", "tensor"), ("mxfp4", "block"), ("nvfp4", "block")]),
     (2, None, [("int8", "row"), ("e4m3", "row"), ("mxfp4", "block"), ("nvfp4", "block")]),
-    (3, None, [("e4m3", "row"), ("e5m2", "row"), ("nvfp4", "block")]),
-    (4, None, [("mxfp4", "block"), ("nvfp4", "block")]),
+    (3, None, [("e4m3", "row"), ("e5m2", "row"), ("nvfp4", "block"), ("nvfp4", "block", "delayed")]),
+    (4, None, [("mxfp4", "block"), ("nvfp4", "block"), ("nvfp4", "block", "delayed")]),
     (5, 4096, [(f, g) for f in ("int8", "e4m3", "e5m2") for g in ("unit", "tensor")] +
-              [(f, g) for f in ("mxfp4", "nvfp4") for g in ("unit", "block")]),
+              [(f, g) for f in ("mxfp4", "nvfp4") for g in ("unit", "block")] +
+              [("e4m3", "tensor", "delayed"), ("nvfp4", "block", "delayed")]),
 ]
 
 
@@ -207,16 +210,26 @@ def measure_matrix(dev, peaks, flush, x4=None, reps=10, which=(1, 2, 3, 4, 5)) -
         eb = x.element_size()
         idt = qz.QZ_BF16 if x.dtype == torch.bfloat16 else qz.QZ_F32
         name = W.WORKLOADS[k]["name"] + ("" if rows is None else f" (first {rows} rows)")
-        for fname, gname in runs:
+        a_in = qz.amax(x, ws)
+        a_out = torch.empty((1,), dtype=torch.float32, device=dev)
+        for run in runs:
+            fname, gname = run[0], run[1]
+            delayed = len(run) > 2
             f, g = qz.FORMATS[fname], qz.GRANULARITIES[gname]
             codes, scales, ts = qz.alloc_outputs(f, g, r, c, dev)
             y = torch.empty((r, c), dtype=x.dtype, device=dev)
             d = qz.make_desc(f, idt, g, r, c)
-            amax_pass = g == qz.QZ_GRAN_TENSOR or (f == qz.QZ_NVFP4 and g == qz.QZ_GRAN_BLOCK)
+            amax_pass = not delayed and (g == qz.QZ_GRAN_TENSOR or
+                                         (f == qz.QZ_NVFP4 and g == qz.QZ_GRAN_BLOCK))
 
             def q():
-                rc = qz.qz_quantize(d, x.data_ptr(), codes.data_ptr(), qz._ptr(scales), ts.data_ptr(),
-                                    None, st.data_ptr(), ws.ptr, sp)
+                if delayed:
+                    rc = qz.qz_quantize_delayed(d, x.data_ptr(), codes.data_ptr(), qz._ptr(scales),
+                                                ts.data_ptr(), a_in.data_ptr(), a_out.data_ptr(),
+                                                st.data_ptr(), ws.ptr, sp)
+                else:
+                    rc = qz.qz_quantize(d, x.data_ptr(), codes.data_ptr(), qz._ptr(scales),
+                                        ts.data_ptr(), None, st.data_ptr(), ws.ptr, sp)
                 assert rc == 0, rc
 
             def dq():
@@ -225,9 +238,10 @@ def measure_matrix(dev, peaks, flush, x4=None, reps=10, which=(1, 2, 3, 4, 5)) -
                 assert rc == 0, rc
             qms, dms = timed(q), timed(dq)
             cb = codes.numel() + (0 if scales is None else scales.numel() * scales.element_size()) + 4
-            qb = n * eb * (2 if amax_pass else 1) + cb + 32
+            qb = n * eb * (2 if amax_pass else 1) + cb + 32 + (8 if delayed else 0)
             db = cb + n * eb
-            out.append({"workload": name, "format": fname, "granularity": gname,
+            out.append({"workload": name, "format": fname,
+                        "granularity": gname + (" delayed" if delayed else ""),
                         "quantize_us": round(qms * 1e3, 1),
                         "quantize_gbs": round(qb / qms / 1e6, 1),
                         "quantize_frac": round(qb / qms / 1e6 / peaks["hbm_gbs"], 3),

@@ -164,6 +164,25 @@ QZ_API qz_status qz_quantize(const qz_desc* desc, const void* x, void* codes, vo
                       float* tensor_scale_dev, const float* tensor_amax_dev,
                       qz_stats* stats_dev, void* ws, qz_stream_t stream);
 
+/* Quantize with a per-tensor scale taken from a previous tensor ("delayed" scaling), and
+ * return this tensor's own amax for the next call.  The post leaves open where NVFP4's
+ * global amax comes from (section "FP4 / MXFP4 / NVFP4"): this is the reading in which it
+ * comes from an earlier step, so the quantize needs no extra read of x.
+ *   amax_in_dev   device fp32, required for TENSOR and NVFP4 BLOCK (else ignored, may be
+ *                 NULL): the alpha of the scale, exactly as tensor_amax_dev of qz_quantize.
+ *                 Elements beyond it saturate, as the formats define.
+ *   amax_out_dev  device fp32, required: max |x| of this tensor, bit-identical to what
+ *                 qz_amax writes (QZ_FLAG_NONFINITE_INPUT on NaN / Inf).  On dense, 16-byte
+ *                 aligned TENSOR / UNIT / BLOCK tensors it is folded into the quantize
+ *                 kernel; elsewhere (ROW, strided or unaligned) it takes a separate read.
+ *                 May alias amax_in_dev: the scale is read before amax_out is written.
+ *   ws            workspace, required.
+ * Everything else as qz_quantize (codes, scales, tensor_scale_dev, stats_dev). */
+QZ_API qz_status qz_quantize_delayed(const qz_desc* desc, const void* x, void* codes, void* scales,
+                                     float* tensor_scale_dev, const float* amax_in_dev,
+                                     float* amax_out_dev, qz_stats* stats_dev, void* ws,
+                                     qz_stream_t stream);
+
 /* Dequantize codes (+ scales, + tensor_scale_dev) into y ([rows, cols], leading dimension
  * desc->ld) of dtype out_dtype.  desc->in_dtype is ignored. */
 QZ_API qz_status qz_dequantize(const qz_desc* desc, const void* codes, const void* scales,

@@ -38,8 +38,8 @@ BLOCK_SIZE = {QZ_MXFP4: 32, QZ_NVFP4: 16}
 
 # Names of the exported C symbols (the whole ABI of include/qz.h).
 ABI_SYMBOLS = ("qz_status_string", "qz_workspace_size", "qz_workspace_init", "qz_amax",
-               "qz_quantize", "qz_dequantize", "qz_error_stats", "qz_error_stats_noalloc",
-               "qz_get_device_status")
+               "qz_quantize", "qz_quantize_delayed", "qz_dequantize", "qz_error_stats",
+               "qz_error_stats_noalloc", "qz_get_device_status")
 
 
 class QzDesc(C.Structure):
@@ -80,6 +80,7 @@ def lib():
             "qz_workspace_init": (i32, [vp, C.c_size_t, vp]),
             "qz_amax": (i32, [dp, vp, vp, vp, vp]),
             "qz_quantize": (i32, [dp, vp, vp, vp, vp, vp, vp, vp, vp]),
+            "qz_quantize_delayed": (i32, [dp, vp, vp, vp, vp, vp, vp, vp, vp, vp]),
             "qz_dequantize": (i32, [dp, vp, vp, vp, vp, i32, vp]),
             "qz_error_stats": (i32, [dp, vp, vp, vp, vp, vp, vp, vp]),
             "qz_error_stats_noalloc": (i32, [dp, vp, vp, vp, vp, vp, vp]),
@@ -114,6 +115,13 @@ def qz_quantize(desc: QzDesc, x: int, codes: int, scales: int | None,
                 stats_dev: int | None, ws: int | None, stream: int = 0) -> int:
     return lib().qz_quantize(C.byref(desc), x, codes, scales, tensor_scale_dev,
                              tensor_amax_dev, stats_dev, ws, stream)
+
+
+def qz_quantize_delayed(desc: QzDesc, x: int, codes: int, scales: int | None,
+                        tensor_scale_dev: int | None, amax_in_dev: int | None, amax_out_dev: int,
+                        stats_dev: int | None, ws: int, stream: int = 0) -> int:
+    return lib().qz_quantize_delayed(C.byref(desc), x, codes, scales, tensor_scale_dev,
+                                     amax_in_dev, amax_out_dev, stats_dev, ws, stream)
 
 
 def qz_dequantize(desc: QzDesc, codes: int, scales: int | None, tensor_scale_dev: int | None,
@@ -290,6 +298,29 @@ def quantize(x, fmt, granularity=None, scale_round: int = QZ_SCALE_UP, tensor_am
                      _stream(stream))
     _check(rc, "qz_quantize")
     return Quantized(codes, scales, tscale, f, g, scale_round, rows, cols), st
+
+
+def quantize_delayed(x, fmt, amax_in, granularity=None, scale_round: int = QZ_SCALE_UP,
+                     stats: bool = False, workspace: Workspace | None = None, out=None,
+                     amax_out=None, stream=None):
+    """Quantize with the per-tensor scale of an earlier tensor's amax (amax_in: fp32 CUDA
+    tensor [1], or None where the granularity needs none) and return this tensor's amax.
+    Returns (Quantized, stats tensor or None, amax_out tensor [1])."""
+    torch = _torch()
+    f = _fmt(fmt)
+    g = default_granularity(f) if granularity is None else _gran(granularity)
+    rows, cols, ld = _rows_cols_ld(x)
+    desc = make_desc(f, _dtype_code(x.dtype), g, rows, cols, ld, scale_round)
+    codes, scales, tscale = out if out is not None else alloc_outputs(f, g, rows, cols, x.device)
+    st = torch.empty((STATS_BYTES,), dtype=torch.uint8, device=x.device) if stats else None
+    workspace = workspace or Workspace(x.device)
+    amax_out = amax_out if amax_out is not None else torch.empty((1,), dtype=torch.float32,
+                                                                 device=x.device)
+    rc = qz_quantize_delayed(desc, x.data_ptr(), codes.data_ptr(), _ptr(scales),
+                             tscale.data_ptr(), _ptr(amax_in), amax_out.data_ptr(), _ptr(st),
+                             workspace.ptr, _stream(stream))
+    _check(rc, "qz_quantize_delayed")
+    return Quantized(codes, scales, tscale, f, g, scale_round, rows, cols), st, amax_out
 
 
 def dequantize(q: Quantized, out_dtype=None, out=None, stream=None):

@@ -104,8 +104,9 @@ bool set_dyn_smem(const void* kernel, int bytes) {
 
 namespace {
 
-__global__ void fill_kernel(float* a, float va, qz_stats* st) {
+__global__ void fill_kernel(float* a, float va, qz_stats* st, float* zero_out = nullptr) {
   if (a) *a = va;
+  if (zero_out) *zero_out = 0.0f;
   if (st) {
     st->sum_sq_err = 0.0;
     st->mse = 0.0;
@@ -244,6 +245,36 @@ extern "C" qz_status qz_quantize(const qz_desc* d, const void* x, void* codes, v
   if (is8(d->format))
     return launch_quant8(*d, x, codes, scales, tensor_scale_dev, amax, !compute_amax, stats_dev, ws, s);
   return launch_quant4(*d, x, codes, scales, tensor_scale_dev, amax, !compute_amax, stats_dev, ws, s);
+}
+
+extern "C" qz_status qz_quantize_delayed(const qz_desc* d, const void* x, void* codes, void* scales,
+                                         float* tensor_scale_dev, const float* amax_in_dev,
+                                         float* amax_out_dev, qz_stats* stats_dev, void* ws,
+                                         qz_stream_t stream) {
+  qz_status st = check_desc(d);
+  if (st != QZ_OK) return st;
+  if ((st = check_dtype(d->in_dtype)) != QZ_OK) return st;
+  const bool tensor_alpha = needs_tscale(d);
+  if (!amax_out_dev || (tensor_alpha && (!amax_in_dev || !tensor_scale_dev))) return QZ_ERR_NULL;
+  if ((st = check_ws(ws)) != QZ_OK) return st;
+  if (!aligned(amax_out_dev, 4) || (amax_in_dev && !aligned(amax_in_dev, 4))) return QZ_ERR_ALIGN;
+  if (tensor_scale_dev && !aligned(tensor_scale_dev, 4)) return QZ_ERR_ALIGN;
+  if (stats_dev && !aligned(stats_dev, 8)) return QZ_ERR_ALIGN;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (d->rows * d->cols == 0) {
+    // an empty tensor's amax is 0, as qz_amax would write
+    fill_kernel<<<1, 1, 0, s>>>(tensor_scale_dev, 1.0f, stats_dev, amax_out_dev);
+    return launch_status();
+  }
+  if (!x || !codes) return QZ_ERR_NULL;
+  if (needs_scales(d) && !scales) return QZ_ERR_NULL;
+  const int eb = d->in_dtype == QZ_BF16 ? 2 : 4;
+  if (!aligned(x, eb)) return QZ_ERR_ALIGN;
+  if (d->granularity == QZ_GRAN_ROW && !aligned(scales, 4)) return QZ_ERR_ALIGN;
+  const float* amax = tensor_alpha ? amax_in_dev : nullptr;
+  if (is8(d->format))
+    return launch_quant8(*d, x, codes, scales, tensor_scale_dev, amax, true, stats_dev, ws, s, amax_out_dev);
+  return launch_quant4(*d, x, codes, scales, tensor_scale_dev, amax, true, stats_dev, ws, s, amax_out_dev);
 }
 
 extern "C" qz_status qz_dequantize(const qz_desc* d, const void* codes, const void* scales,

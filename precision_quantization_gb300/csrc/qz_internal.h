@@ -29,12 +29,14 @@ bool set_dyn_smem(const void* kernel, int bytes);
 
 qz_status launch_amax(const qz_desc& d, const void* x, float* out, void* ws, cudaStream_t s);
 
+// amax_out (may be null): also write this tensor's max |x|, bit-identical to launch_amax --
+// folded into the staged kernels, a separate amax pass elsewhere.
 qz_status launch_quant8(const qz_desc& d, const void* x, void* codes, void* scales,
                         float* tscale_out, const float* amax, bool amax_supplied,
-                        qz_stats* stats, void* ws, cudaStream_t s);
+                        qz_stats* stats, void* ws, cudaStream_t s, float* amax_out = nullptr);
 qz_status launch_quant4(const qz_desc& d, const void* x, void* codes, void* scales,
                         float* tscale_out, const float* amax, bool amax_supplied,
-                        qz_stats* stats, void* ws, cudaStream_t s);
+                        qz_stats* stats, void* ws, cudaStream_t s, float* amax_out = nullptr);
 qz_status launch_dequant8(const qz_desc& d, const void* codes, const void* scales,
                           const float* tscale, void* y, int out_dtype, cudaStream_t s);
 qz_status launch_dequant4(const qz_desc& d, const void* codes, const void* scales,

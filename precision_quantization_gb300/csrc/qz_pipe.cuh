@@ -251,6 +251,48 @@ __device__ __forceinline__ void acc_pairs(StatAcc& acc, const uint64_t (&xp)[NP]
   }
 }
 
+// CTA maximum of per-thread maxima (m: bf16 -> two 16-bit magnitudes, fp32 -> one), written
+// as this CTA's partial; the last CTA to finish folds the partials into *out and flags a
+// non-finite maximum.
+template <int DT>
+__device__ __forceinline__ void amax_finish(uint32_t m, float* out, void* ws) {
+  uint32_t bits;  // fp32 bit pattern of this thread's maximum
+  if constexpr (DT == QZ_BF16) bits = max(m & 0xffffu, m >> 16) << 16;
+  else bits = m;
+#pragma unroll
+  for (int o = 16; o; o >>= 1) bits = max(bits, __shfl_xor_sync(kFull, bits, o));
+  __shared__ uint32_t s_w[kWarps];
+  __shared__ bool s_last;
+  if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = bits;
+  __syncthreads();
+  float* parts = ws_amax_partials(ws);
+  if (threadIdx.x == 0) {
+    uint32_t b = 0;
+    for (int w = 0; w < kWarps; ++w) b = max(b, s_w[w]);
+    reinterpret_cast<uint32_t*>(parts)[blockIdx.x] = b;
+    __threadfence();
+    const uint32_t done = atomicInc(&ws_header(ws)->amax_counter, gridDim.x - 1);
+    s_last = (done == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  uint32_t b = 0;
+  for (int i = threadIdx.x; i < static_cast<int>(gridDim.x); i += kThreads)
+    b = max(b, reinterpret_cast<volatile uint32_t*>(parts)[i]);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) b = max(b, __shfl_xor_sync(kFull, b, o));
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = b;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t t = 0;
+    for (int w = 0; w < kWarps; ++w) t = max(t, s_w[w]);
+    if (t >= 0x7f800000u) atomicOr(&ws_header(ws)->status, QZ_FLAG_NONFINITE_INPUT);
+    *out = __uint_as_float(t);
+  }
+}
+
 // ---------------------------------------------------------------------------------------
 // mbarrier + bulk copy global -> shared
 // ---------------------------------------------------------------------------------------

@@ -28,6 +28,7 @@ struct Q4Args {
   int scale_round;
   bool reverse;  // pipelined path: walk the tiles from the end of the tensor
   float zero;    // 0.0f, opaque to the assembler (see mul2_rounded)
+  float* amax_out = nullptr;  // staged path: this tensor's max |x| (for the next call's scale)
 };
 
 // fl32(a / b) for scalar scale arithmetic: the FMA-corrected quotient where it is exact
@@ -246,10 +247,11 @@ struct Q4Ctx {
 
 // One 32-byte chunk: block amax, scale, quotients, cast, stores, and (STATS) the error of
 // the chunk.  REL: the exact max |e|/|x| search is still open for this warp (T < 1).
+// am: running max of the block amaxes' bits (the tensor amax, for amax_out).
 template <int FMT, int DT, bool UNIT, bool STATS, int SR, bool REL>
 __device__ __forceinline__ void q4_chunk(const Q4Args& a, const Q4Ctx& cx, const uint32_t (&w)[8],
                                          int64_t u, bool valid, int lane, StatAcc& acc,
-                                         float& tpart) {
+                                         float& tpart, uint32_t& am) {
   constexpr int EPC = Elem<DT>::kPer32B;
   constexpr int BS = FMT == QZ_MXFP4 ? 32 : 16;
   constexpr int L = BS / EPC;
@@ -265,6 +267,7 @@ __device__ __forceinline__ void q4_chunk(const Q4Args& a, const Q4Ctx& cx, const
   if constexpr (L >= 2) A = absmax_nan(A, __shfl_xor_sync(kFull, A, 1));
   if constexpr (L >= 4) A = absmax_nan(A, __shfl_xor_sync(kFull, A, 2));
   if (valid && !is_finite_f(A)) flag_status(a.ws, QZ_FLAG_NONFINITE_INPUT);
+  am = max(am, __float_as_uint(A));  // A >= 0; lanes without data hold 0
 
   // block scale s and the quotients v = fl32(x / s), as fp32 pairs
   uint32_t scode;
@@ -422,6 +425,7 @@ __global__ void __launch_bounds__(kThreads, 3) quant4_pipe_kernel(Q4Args a) {
   if (tid == 0) P.prologue();
 
   StatAcc acc;
+  uint32_t am = 0u;
   for (int64_t k = 0; P.has(k); ++k) {
     const int64_t tile = P.tile_of(k);
     if (!P.wait(k)) s_abort = 1;
@@ -440,9 +444,9 @@ __global__ void __launch_bounds__(kThreads, 3) quant4_pipe_kernel(Q4Args a) {
         for (int i = 0; i < 8; ++i) w[i] = 0u;
       }
       if (!STATS || acc.T >= 1.0f)  // warp-uniform: the relative-error search is settled
-        q4_chunk<FMT, DT, UNIT, STATS, SR, false>(a, cx, w, u, valid, lane, acc, tpart);
+        q4_chunk<FMT, DT, UNIT, STATS, SR, false>(a, cx, w, u, valid, lane, acc, tpart, am);
       else
-        q4_chunk<FMT, DT, UNIT, STATS, SR, true>(a, cx, w, u, valid, lane, acc, tpart);
+        q4_chunk<FMT, DT, UNIT, STATS, SR, true>(a, cx, w, u, valid, lane, acc, tpart, am);
     }
     if constexpr (STATS) acc_add_sum(acc, tpart);
     __syncthreads();  // every thread is done with this stage
@@ -455,6 +459,7 @@ __global__ void __launch_bounds__(kThreads, 3) quant4_pipe_kernel(Q4Args a) {
     }
     if (tid == 0) P.issue(k + kStages);
   }
+  if (a.amax_out) amax_finish<QZ_F32>(am, a.amax_out, a.ws);
   if constexpr (STATS) stats_finish(acc, a.ws, a.stats, static_cast<uint64_t>(a.g.rows * a.g.cols));
 }
 
@@ -470,11 +475,15 @@ qz_status run_pipe(const Q4Args& args, cudaStream_t s) {
   return launch_status();
 }
 
+// With amax_out, the staged kernel folds the tensor amax in; the direct path leaves it to
+// the caller (fused: returned true).
 template <int FMT, int DT, bool UNIT, bool STATS, bool VEC>
-qz_status run(const Q4Args& args, cudaStream_t s) {
+qz_status run(const Q4Args& args, cudaStream_t s, bool& fused) {
   if constexpr (VEC) {
-    if (args.g.dense && reinterpret_cast<uintptr_t>(args.x) % 16 == 0)
+    if (args.g.dense && reinterpret_cast<uintptr_t>(args.x) % 16 == 0) {
+      fused = true;
       return run_pipe<FMT, DT, UNIT, STATS>(args, s);
+    }
   }
   auto kern = &quant4_kernel<FMT, DT, UNIT, STATS, VEC>;
   const int64_t per_cta = static_cast<int64_t>(kThreads) * kUnroll;
@@ -484,21 +493,21 @@ qz_status run(const Q4Args& args, cudaStream_t s) {
 }
 
 template <int FMT, int DT>
-qz_status dispatch(const Q4Args& args, bool unit, bool stats, cudaStream_t s) {
+qz_status dispatch(const Q4Args& args, bool unit, bool stats, cudaStream_t s, bool& f) {
   const bool vec = args.g.vec;
   if (unit) {
-    if (stats) return vec ? run<FMT, DT, true, true, true>(args, s) : run<FMT, DT, true, true, false>(args, s);
-    return vec ? run<FMT, DT, true, false, true>(args, s) : run<FMT, DT, true, false, false>(args, s);
+    if (stats) return vec ? run<FMT, DT, true, true, true>(args, s, f) : run<FMT, DT, true, true, false>(args, s, f);
+    return vec ? run<FMT, DT, true, false, true>(args, s, f) : run<FMT, DT, true, false, false>(args, s, f);
   }
-  if (stats) return vec ? run<FMT, DT, false, true, true>(args, s) : run<FMT, DT, false, true, false>(args, s);
-  return vec ? run<FMT, DT, false, false, true>(args, s) : run<FMT, DT, false, false, false>(args, s);
+  if (stats) return vec ? run<FMT, DT, false, true, true>(args, s, f) : run<FMT, DT, false, true, false>(args, s, f);
+  return vec ? run<FMT, DT, false, false, true>(args, s, f) : run<FMT, DT, false, false, false>(args, s, f);
 }
 
 }  // namespace
 
 qz_status launch_quant4(const qz_desc& d, const void* x, void* codes, void* scales,
                         float* tscale_out, const float* amax, bool /*amax_supplied*/,
-                        qz_stats* stats, void* ws, cudaStream_t s) {
+                        qz_stats* stats, void* ws, cudaStream_t s, float* amax_out) {
   const int eb = d.in_dtype == QZ_BF16 ? 2 : 4;
   Q4Args args;
   args.x = x;
@@ -519,13 +528,19 @@ qz_status launch_quant4(const qz_desc& d, const void* x, void* codes, void* scal
   // starting from the end of x picks up what that read left in L2
   args.reverse = d.format == QZ_NVFP4 && d.granularity == QZ_GRAN_BLOCK;
   args.zero = 0.0f;
+  args.amax_out = amax_out;
   const bool unit = d.granularity == QZ_GRAN_UNIT;
   const bool st = stats != nullptr;
+  bool fused = false;
+  qz_status rc;
   if (d.format == QZ_MXFP4)
-    return d.in_dtype == QZ_BF16 ? dispatch<QZ_MXFP4, QZ_BF16>(args, unit, st, s)
-                                 : dispatch<QZ_MXFP4, QZ_F32>(args, unit, st, s);
-  return d.in_dtype == QZ_BF16 ? dispatch<QZ_NVFP4, QZ_BF16>(args, unit, st, s)
-                               : dispatch<QZ_NVFP4, QZ_F32>(args, unit, st, s);
+    rc = d.in_dtype == QZ_BF16 ? dispatch<QZ_MXFP4, QZ_BF16>(args, unit, st, s, fused)
+                               : dispatch<QZ_MXFP4, QZ_F32>(args, unit, st, s, fused);
+  else
+    rc = d.in_dtype == QZ_BF16 ? dispatch<QZ_NVFP4, QZ_BF16>(args, unit, st, s, fused)
+                               : dispatch<QZ_NVFP4, QZ_F32>(args, unit, st, s, fused);
+  if (rc == QZ_OK && amax_out && !fused) rc = launch_amax(d, x, amax_out, ws, s);
+  return rc;
 }
 
 }  // namespace qz

@@ -24,6 +24,7 @@ struct Q8Args {
   float* tscale_out;
   qz_stats* stats;
   void* ws;
+  float* amax_out = nullptr;  // staged per-tensor-supplied / unit path: this tensor's max |x|
 };
 
 // Load chunk u = (row, chunk index j) of x into w (zero-filled past the end of the row).
@@ -301,11 +302,12 @@ __device__ __forceinline__ void q8_cast(const uint64_t (&vp)[NP], uint32_t (&cw)
   }
 }
 
-// One chunk of the per-tensor / unit-scale path: quotients, cast, store, stats.
+// One chunk of the per-tensor / unit-scale path: quotients, cast, store, stats.  am: running
+// max of the chunk amaxes' bits (MODE != kTensorComputed; the tensor amax for amax_out).
 template <int FMT, int DT, int MODE, bool STATS, bool REL>
 __device__ __forceinline__ void q8_chunk(const uint32_t (&w)[8], bool valid, uint8_t* cp, float s,
                                          uint64_t r2, uint64_t ns2, uint64_t s2, uint64_t z2, bool fast,
-                                         void* ws, StatAcc& acc, float& tpart) {
+                                         void* ws, StatAcc& acc, float& tpart, uint32_t& am) {
   constexpr int EPC = Elem<DT>::kPer32B;
   constexpr int NP = EPC / 2;
   uint64_t xp[NP];
@@ -326,6 +328,7 @@ __device__ __forceinline__ void q8_chunk(const uint32_t (&w)[8], bool valid, uin
       A = absmax3(A, a, b);
     }
     if (valid && !is_finite_f(A)) flag_status(ws, QZ_FLAG_NONFINITE_INPUT);
+    am = max(am, __float_as_uint(A));
     if constexpr (MODE == kTensorSupplied) {
       float r, rr;
       upk(r2, r, rr);
@@ -406,6 +409,7 @@ __global__ void __launch_bounds__(kThreads, 3) quant8_pipe_kernel(Q8Args a, floa
                                                 false};
   if (tid == 0) P.prologue();
   StatAcc acc;
+  uint32_t am = 0u;
   for (int64_t k = 0; P.has(k); ++k) {
     const int64_t tile = P.tile_of(k);
     if (!P.wait(k)) s_abort = 1;
@@ -425,9 +429,9 @@ __global__ void __launch_bounds__(kThreads, 3) quant8_pipe_kernel(Q8Args a, floa
       }
       uint8_t* cp = a.codes + u * EPC;
       if (!STATS || acc.T >= 1.0f)  // warp-uniform: the relative-error search is settled
-        q8_chunk<FMT, DT, MODE, STATS, false>(w, valid, cp, s, r2, ns2, s2, z2, fast, a.ws, acc, tpart);
+        q8_chunk<FMT, DT, MODE, STATS, false>(w, valid, cp, s, r2, ns2, s2, z2, fast, a.ws, acc, tpart, am);
       else
-        q8_chunk<FMT, DT, MODE, STATS, true>(w, valid, cp, s, r2, ns2, s2, z2, fast, a.ws, acc, tpart);
+        q8_chunk<FMT, DT, MODE, STATS, true>(w, valid, cp, s, r2, ns2, s2, z2, fast, a.ws, acc, tpart, am);
     }
     if constexpr (STATS) acc_add_sum(acc, tpart);
     __syncthreads();
@@ -439,6 +443,9 @@ __global__ void __launch_bounds__(kThreads, 3) quant8_pipe_kernel(Q8Args a, floa
       return;
     }
     if (tid == 0) P.issue(k + kPipeStages);
+  }
+  if constexpr (MODE != kTensorComputed) {
+    if (a.amax_out) amax_finish<QZ_F32>(am, a.amax_out, a.ws);
   }
   if constexpr (STATS) stats_finish(acc, a.ws, a.stats, static_cast<uint64_t>(a.g.rows * a.g.cols));
 }
@@ -523,6 +530,7 @@ __global__ void __launch_bounds__(kThreads) quant8_rowpipe_kernel(Q8Args a, floa
     const uint64_t r2 = pk(r, r), ns2 = pk(-s, -s), s2 = pk(s, s);
     // pass 2: codes (warp-uniform trip count: the stats vote)
     float tpart = 0.0f;
+    uint32_t am_unused = 0u;
     uint8_t* crow = a.codes + row * g.cols;
     for (int64_t jb = tid & ~31; jb < g.cpr; jb += kThreads) {
       const int64_t j = jb + lane;
@@ -536,10 +544,10 @@ __global__ void __launch_bounds__(kThreads) quant8_rowpipe_kernel(Q8Args a, floa
       }
       if (!STATS || acc.T >= 1.0f)
         q8_chunk<FMT, DT, kTensorComputed, STATS, false>(w, valid, crow + j * EPC, s, r2, ns2, s2, z2,
-                                                         fast, a.ws, acc, tpart);
+                                                         fast, a.ws, acc, tpart, am_unused);
       else
         q8_chunk<FMT, DT, kTensorComputed, STATS, true>(w, valid, crow + j * EPC, s, r2, ns2, s2, z2,
-                                                        fast, a.ws, acc, tpart);
+                                                        fast, a.ws, acc, tpart, am_unused);
     }
     if constexpr (STATS) acc_add_sum(acc, tpart);
     __syncthreads();  // stage and s_red free again
@@ -591,8 +599,9 @@ qz_status run_row(const Q8Args& args, cudaStream_t s) {
 }
 
 template <int FMT, int DT, int MODE, bool STATS>
-qz_status run_flat(const Q8Args& args, cudaStream_t s) {
+qz_status run_flat(const Q8Args& args, cudaStream_t s, bool& fused) {
   if (args.g.vec && args.g.dense && reinterpret_cast<uintptr_t>(args.x) % 16 == 0) {
+    fused = MODE != kTensorComputed;
     auto kern = &quant8_pipe_kernel<FMT, DT, MODE, STATS>;
     if (!set_dyn_smem(reinterpret_cast<const void*>(kern), static_cast<int>(kPipeSmem)))
       return QZ_ERR_CUDA;
@@ -608,28 +617,29 @@ qz_status run_flat(const Q8Args& args, cudaStream_t s) {
 }
 
 template <int FMT, int DT>
-qz_status dispatch(const Q8Args& args, int gran, bool supplied, bool stats, cudaStream_t s) {
+qz_status dispatch(const Q8Args& args, int gran, bool supplied, bool stats, cudaStream_t s, bool& f) {
   if (gran == QZ_GRAN_ROW) return stats ? run_row<FMT, DT, true>(args, s) : run_row<FMT, DT, false>(args, s);
   if (gran == QZ_GRAN_UNIT)
-    return stats ? run_flat<FMT, DT, kUnit, true>(args, s) : run_flat<FMT, DT, kUnit, false>(args, s);
+    return stats ? run_flat<FMT, DT, kUnit, true>(args, s, f) : run_flat<FMT, DT, kUnit, false>(args, s, f);
   if (supplied)
-    return stats ? run_flat<FMT, DT, kTensorSupplied, true>(args, s)
-                 : run_flat<FMT, DT, kTensorSupplied, false>(args, s);
-  return stats ? run_flat<FMT, DT, kTensorComputed, true>(args, s)
-               : run_flat<FMT, DT, kTensorComputed, false>(args, s);
+    return stats ? run_flat<FMT, DT, kTensorSupplied, true>(args, s, f)
+                 : run_flat<FMT, DT, kTensorSupplied, false>(args, s, f);
+  return stats ? run_flat<FMT, DT, kTensorComputed, true>(args, s, f)
+               : run_flat<FMT, DT, kTensorComputed, false>(args, s, f);
 }
 
 template <int FMT>
-qz_status dispatch_dt(const qz_desc& d, const Q8Args& args, bool supplied, bool stats, cudaStream_t s) {
-  return d.in_dtype == QZ_BF16 ? dispatch<FMT, QZ_BF16>(args, d.granularity, supplied, stats, s)
-                               : dispatch<FMT, QZ_F32>(args, d.granularity, supplied, stats, s);
+qz_status dispatch_dt(const qz_desc& d, const Q8Args& args, bool supplied, bool stats, cudaStream_t s,
+                      bool& f) {
+  return d.in_dtype == QZ_BF16 ? dispatch<FMT, QZ_BF16>(args, d.granularity, supplied, stats, s, f)
+                               : dispatch<FMT, QZ_F32>(args, d.granularity, supplied, stats, s, f);
 }
 
 }  // namespace
 
 qz_status launch_quant8(const qz_desc& d, const void* x, void* codes, void* scales,
                         float* tscale_out, const float* amax, bool amax_supplied,
-                        qz_stats* stats, void* ws, cudaStream_t s) {
+                        qz_stats* stats, void* ws, cudaStream_t s, float* amax_out) {
   const int eb = d.in_dtype == QZ_BF16 ? 2 : 4;
   Q8Args args;
   args.x = x;
@@ -645,12 +655,17 @@ qz_status launch_quant8(const qz_desc& d, const void* x, void* codes, void* scal
   args.tscale_out = tscale_out;
   args.stats = stats;
   args.ws = ws;
+  args.amax_out = amax_out;
   const bool st = stats != nullptr;
+  bool fused = false;
+  qz_status rc;
   switch (d.format) {
-    case QZ_INT8: return dispatch_dt<QZ_INT8>(d, args, amax_supplied, st, s);
-    case QZ_FP8_E4M3: return dispatch_dt<QZ_FP8_E4M3>(d, args, amax_supplied, st, s);
-    default: return dispatch_dt<QZ_FP8_E5M2>(d, args, amax_supplied, st, s);
+    case QZ_INT8: rc = dispatch_dt<QZ_INT8>(d, args, amax_supplied, st, s, fused); break;
+    case QZ_FP8_E4M3: rc = dispatch_dt<QZ_FP8_E4M3>(d, args, amax_supplied, st, s, fused); break;
+    default: rc = dispatch_dt<QZ_FP8_E5M2>(d, args, amax_supplied, st, s, fused); break;
   }
+  if (rc == QZ_OK && amax_out && !fused) rc = launch_amax(d, x, amax_out, ws, s);
+  return rc;
 }
 
 }  // namespace qz

@@ -121,6 +121,25 @@ def test_quantize_null_and_workspace_errors(qz):
     assert qz.qz_quantize(d_bad, FAKE, FAKE, FAKE, FAKE, None, None, FAKE) == qz.QZ_ERR_UNSUPPORTED
 
 
+def test_quantize_delayed_argument_errors(qz):
+    qd = qz.qz_quantize_delayed
+    d = qz.make_desc("nvfp4", qz.QZ_BF16, "block", 4, 64)
+    # amax_out is required; NVFP4 BLOCK also needs amax_in and the tensor-scale output
+    assert qd(d, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, FAKE) == qz.QZ_ERR_NULL
+    assert qd(d, FAKE, FAKE, FAKE, FAKE, None, FAKE, None, FAKE) == qz.QZ_ERR_NULL
+    assert qd(d, FAKE, FAKE, FAKE, None, FAKE, FAKE, None, FAKE) == qz.QZ_ERR_NULL
+    # the workspace is always required (the amax of this tensor is folded through it)
+    assert qd(d, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == qz.QZ_ERR_WORKSPACE
+    assert qd(d, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE + 2, None, FAKE) == qz.QZ_ERR_ALIGN
+    # MXFP4 BLOCK and ROW scales need no amax_in
+    d_mx = qz.make_desc("mxfp4", qz.QZ_BF16, "block", 4, 64)
+    assert qd(d_mx, None, FAKE, FAKE, None, None, FAKE, None, FAKE) == qz.QZ_ERR_NULL  # x
+    d_row = qz.make_desc("e4m3", qz.QZ_F32, "row", 4, 64)
+    assert qd(d_row, FAKE, FAKE, None, None, None, FAKE, None, FAKE) == qz.QZ_ERR_NULL  # scales
+    assert qz.lib().qz_quantize_delayed(None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE,
+                                        None) == qz.QZ_ERR_NULL
+
+
 def test_dequantize_and_stats_argument_errors(qz):
     d = qz.make_desc("mxfp4", qz.QZ_BF16, "block", 4, 64)
     assert qz.qz_dequantize(d, FAKE, FAKE, None, FAKE, 5) == qz.QZ_ERR_ENUM
