@@ -1,8 +1,9 @@
 """Python view of the CPU oracle (ctypes over ``liboracle.so``).
 
 TEST INFRASTRUCTURE ONLY.  The oracle is the plain CPU definition of what the CUDA
-library must compute bit for bit: quantize to INT8 / FP8 E4M3 / FP8 E5M2 / MXFP4 / NVFP4,
-dequantize, and the error statistics, as described in the blog post
+library must compute bit for bit: quantize to INT8 / FP8 E4M3 / FP8 E5M2 / MXFP4 / NVFP4 /
+INT4, dequantize (also the asymmetric 4-bit group form of the blog's "Puzzles 12"), and the
+error statistics, as described in the blog post
 "浅谈低精度浮点数" (A brief talk on low-precision floats).  Only the tests,
 ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may import it.
 
@@ -18,7 +19,7 @@ import numpy as np
 
 from . import build as _build
 
-INT8, E4M3, E5M2, MXFP4, NVFP4 = 1, 2, 3, 4, 5
+INT8, E4M3, E5M2, MXFP4, NVFP4, INT4 = 1, 2, 3, 4, 5, 6
 E2M1, E8M0 = 16, 17
 BF16, F32 = 1, 2
 GRAN_TENSOR, GRAN_ROW, GRAN_BLOCK, GRAN_UNIT = 1, 2, 3, 4
@@ -71,6 +72,7 @@ def lib():
             "orc_dequantize": (i32, [i32, i32, i32, i64, i64, i64, vp, vp, fp, vp, i32, i32]),
             "orc_error_stats": (i32, [i32, i32, i32, i32, i64, i64, i64, vp, vp, vp, fp, sp,
                                       i32]),
+            "orc_dequant_asym4": (i32, [i64, i64, i64, vp, vp, vp, vp, i32, i32]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -152,10 +154,13 @@ def _check(rc: int, what: str):
 
 
 def code_bytes(fmt: int, rows: int, cols: int) -> int:
-    return rows * cols // 2 if fmt in (MXFP4, NVFP4) else rows * cols
+    return rows * cols // 2 if fmt in (MXFP4, NVFP4, INT4) else rows * cols
 
 
-def block_of(fmt: int) -> int:
+def block_of(fmt: int, block_size: int | None = None) -> int:
+    """Block (group) size: fixed for MXFP4 / NVFP4, chosen for INT4 (default 32)."""
+    if fmt == INT4:
+        return 32 if block_size is None else block_size
     return {MXFP4: 32, NVFP4: 16}.get(fmt, 0)
 
 
@@ -168,17 +173,20 @@ def amax(x: np.ndarray, nthreads: int = 0) -> float:
 
 
 def quantize(x: np.ndarray, fmt: int, granularity: int, scale_round: int = SCALE_UP,
-             tensor_amax=None, stats: bool = False, nthreads: int = 0):
+             tensor_amax=None, stats: bool = False, nthreads: int = 0,
+             block_size: int | None = None):
     """Return (codes uint8, scales, tensor_scale float32, Stats or None).
 
-    codes: [rows, cols] (8-bit formats) or [rows, cols/2] (FP4, low nibble first);
-    scales: float32 [rows] for ROW, uint8 [rows, cols/bs] for MXFP4/NVFP4, else None.
+    codes: [rows, cols] (8-bit formats) or [rows, cols/2] (4-bit, low nibble first);
+    scales: float32 [rows] for ROW, uint8 [rows, cols/bs] for MXFP4/NVFP4, float32
+    [rows, cols/bs] for INT4, else None.
     """
     rows, cols, ld = _rows_cols_ld(x)
-    bs = block_of(fmt)
+    bs = block_of(fmt, block_size)
     codes = np.zeros((rows, cols // 2 if bs else cols), dtype=np.uint8)
     if bs:
-        scales = np.zeros((rows, cols // bs if bs else 0), dtype=np.uint8)
+        scales = np.zeros((rows, cols // bs if bs else 0),
+                          dtype=np.float32 if fmt == INT4 else np.uint8)
     elif granularity == GRAN_ROW:
         scales = np.zeros((rows,), dtype=np.float32)
     else:
@@ -197,8 +205,9 @@ def quantize(x: np.ndarray, fmt: int, granularity: int, scale_round: int = SCALE
 
 
 def dequantize(codes: np.ndarray, scales, tensor_scale, fmt: int, granularity: int,
-               rows: int, cols: int, out_dtype: int = BF16, nthreads: int = 0):
-    bs = block_of(fmt)
+               rows: int, cols: int, out_dtype: int = BF16, nthreads: int = 0,
+               block_size: int | None = None):
+    bs = block_of(fmt, block_size)
     y = np.zeros((rows, cols), dtype=np.uint16 if out_dtype == BF16 else np.float32)
     ts = C.c_float(float(tensor_scale if tensor_scale is not None else 1.0))
     rc = lib().orc_dequantize(fmt, granularity, bs, rows, cols, cols, _ptr(codes),
@@ -208,9 +217,9 @@ def dequantize(codes: np.ndarray, scales, tensor_scale, fmt: int, granularity: i
 
 
 def error_stats(x: np.ndarray, codes: np.ndarray, scales, tensor_scale, fmt: int,
-                granularity: int, nthreads: int = 0) -> Stats:
+                granularity: int, nthreads: int = 0, block_size: int | None = None) -> Stats:
     rows, cols, ld = _rows_cols_ld(x)
-    bs = block_of(fmt)
+    bs = block_of(fmt, block_size)
     ts = C.c_float(float(tensor_scale if tensor_scale is not None else 1.0))
     st = _Stats()
     rc = lib().orc_error_stats(fmt, _dtype_of(x), granularity, bs, rows, cols, ld, _ptr(x),
@@ -219,3 +228,19 @@ def error_stats(x: np.ndarray, codes: np.ndarray, scales, tensor_scale, fmt: int
     _check(rc, "error_stats")
     return Stats(st.sum_sq_err, st.mse, np.float32(st.max_rel_err),
                  np.float32(st.max_abs_err), int(st.n))
+
+
+def dequant_asym4(w: np.ndarray, scales: np.ndarray, shifts: np.ndarray, rows: int, cols: int,
+                  group: int, out_dtype: int = F32, nthreads: int = 0):
+    """Asymmetric 4-bit group dequantization of the "Puzzles 12" section:
+    y = sc * (w - sh).  w: uint32 [rows, cols/8]; scales: float32 [rows, cols/group];
+    shifts: uint32 [rows, ceil(cols/group/8)]; nibbles low first.  Returns y as bf16 bits
+    (uint16) or float32."""
+    y = np.zeros((rows, cols), dtype=np.uint16 if out_dtype == BF16 else np.float32)
+    w = np.ascontiguousarray(w, dtype=np.uint32)
+    scales = np.ascontiguousarray(scales, dtype=np.float32)
+    shifts = np.ascontiguousarray(shifts, dtype=np.uint32)
+    rc = lib().orc_dequant_asym4(rows, cols, group, _ptr(w), _ptr(scales), _ptr(shifts),
+                                 _ptr(y), out_dtype, nthreads)
+    _check(rc, "dequant_asym4")
+    return y

@@ -134,6 +134,14 @@ static double dec_int8(uint32_t c) {
   return (double)v;
 }
 
+/* INT4: a 4-bit two's complement nibble ("FP4 / MXFP4 / NVFP4", last paragraph: symmetric
+ * INT4 with q in [-7, 7]); the pattern 1000 (-8) is decodable but never produced */
+static double dec_int4(uint32_t c) {
+  int v = (int)(c & 0xFu);
+  if (v >= 8) v -= 16;
+  return (double)v;
+}
+
 static double dec_e4m3(uint32_t c) { /* bias 7, no Inf, S.1111.111 = NaN */
   const int s = (int)((c >> 7) & 1u), e = (int)((c >> 3) & 0xFu), m = (int)(c & 7u);
   double mag;
@@ -178,6 +186,7 @@ static double dec_e8m0(uint32_t c) { /* power of two, bias 127, 255 = NaN */
 double orc_decode_code(int fmt, uint32_t code) {
   switch (fmt) {
     case ORC_INT8: return dec_int8(code);
+    case ORC_INT4: return dec_int4(code);
     case ORC_E4M3: return dec_e4m3(code);
     case ORC_E5M2: return dec_e5m2(code);
     case ORC_E2M1: return dec_e2m1(code);
@@ -193,7 +202,7 @@ typedef struct {
   uint32_t code[128];
 } grid_t;
 
-static grid_t G_INT8, G_E4M3, G_E5M2, G_E2M1;
+static grid_t G_INT8, G_INT4, G_E4M3, G_E5M2, G_E2M1;
 static int grids_ready = 0;
 
 static void fill_grid(grid_t* g, int fmt, uint32_t ncodes) {
@@ -215,6 +224,7 @@ static void init_grids(void) {
   {
     if (!grids_ready) {
       fill_grid(&G_INT8, ORC_INT8, 128); /* 0..127: q in [-127, 127] */
+      fill_grid(&G_INT4, ORC_INT4, 8);   /* 0..7: q in [-7, 7] */
       fill_grid(&G_E4M3, ORC_E4M3, 128);
       fill_grid(&G_E5M2, ORC_E5M2, 128);
       fill_grid(&G_E2M1, ORC_E2M1, 8);
@@ -226,6 +236,7 @@ static void init_grids(void) {
 static const grid_t* grid_of(int fmt) {
   switch (fmt) {
     case ORC_INT8: return &G_INT8;
+    case ORC_INT4: return &G_INT4;
     case ORC_E4M3: return &G_E4M3;
     case ORC_E5M2: return &G_E5M2;
     case ORC_E2M1:
@@ -258,6 +269,7 @@ static uint32_t encode_value(int fmt, double v) {
   const int neg = signbit(v) ? 1 : 0;
   const uint32_t mag = g->code[nearest_index(g, fabs(v))];
   if (fmt == ORC_INT8) return neg ? ((256u - mag) & 0xFFu) : mag;
+  if (fmt == ORC_INT4) return neg ? ((16u - mag) & 0xFu) : mag; /* one zero, like INT8 */
   if (fmt == ORC_E4M3 || fmt == ORC_E5M2) return mag | (neg ? 0x80u : 0u);
   return mag | (neg ? 0x8u : 0u); /* E2M1 nibble */
 }
@@ -371,6 +383,11 @@ static int check_shape(int format, int granularity, int block_size, int64_t rows
     if (granularity != ORC_GRAN_TENSOR && granularity != ORC_GRAN_ROW &&
         granularity != ORC_GRAN_UNIT)
       return ORC_ERR_ARG;
+  } else if (format == ORC_INT4) {
+    if (granularity != ORC_GRAN_BLOCK) return ORC_ERR_ARG;
+    if (block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128)
+      return ORC_ERR_ARG;
+    if (cols % block_size) return ORC_ERR_ARG;
   } else if (format == ORC_MXFP4 || format == ORC_NVFP4) {
     const int bs = (format == ORC_MXFP4) ? 32 : 16;
     if (block_size != bs) return ORC_ERR_ARG;
@@ -477,9 +494,9 @@ static float tensor_scale_of(int format, int granularity, float alpha) {
 /* ------------------------------------------------------------------------------------ */
 
 /* One row; acc may be NULL. */
-static void quantize_row(int format, int dt, int granularity, int scale_round, int64_t r,
-                         int64_t cols, int64_t ld, const void* x, void* codes, void* scales,
-                         float tscale, row_acc* acc) {
+static void quantize_row(int format, int dt, int granularity, int scale_round, int block_size,
+                         int64_t r, int64_t cols, int64_t ld, const void* x, void* codes,
+                         void* scales, float tscale, row_acc* acc) {
   const int64_t xo = r * ld;
   if (is8bit(format)) {
     float s;
@@ -500,6 +517,26 @@ static void quantize_row(int format, int dt, int granularity, int scale_round, i
       const uint32_t q = encode_value(format, (double)v);
       put_byte(codes, r * cols + c, q);
       if (acc) acc_elem(acc, xv, (float)orc_decode_code(format, q) * s);
+    }
+    return;
+  }
+  if (format == ORC_INT4) { /* symmetric INT4: s = A / 7 per group (R6 for A = 0) */
+    const int64_t nb = cols / block_size, co = r * (cols / 2);
+    for (int64_t b = 0; b < nb; ++b) {
+      float A = 0.0f;
+      for (int i = 0; i < block_size; ++i) {
+        const float v = fabsf(load_x(x, dt, xo + b * block_size + i));
+        if (v > A) A = v;
+      }
+      const float s = scale_from_amax(A, 7.0f);
+      put_f32(scales, r * nb + b, s);
+      for (int i = 0; i < block_size; ++i) {
+        const int64_t c = b * block_size + i;
+        const float xv = load_x(x, dt, xo + c);
+        const uint32_t q = encode_value(ORC_INT4, (double)(xv / s));
+        put_nibble(codes, co, c, q);
+        if (acc) acc_elem(acc, xv, (float)dec_int4(q) * s);
+      }
     }
     return;
   }
@@ -552,8 +589,8 @@ int orc_quantize(int format, int in_dtype, int granularity, int block_size, int 
   if (scale_round != ORC_SCALE_UP && scale_round != ORC_SCALE_NEAREST) return ORC_ERR_ARG;
   const int64_t n = rows * cols;
   const int nt = nthreads_of(nthreads);
-  const int need_scales =
-      (granularity == ORC_GRAN_ROW) || format == ORC_MXFP4 || format == ORC_NVFP4;
+  const int need_scales = (granularity == ORC_GRAN_ROW) || format == ORC_MXFP4 ||
+                          format == ORC_NVFP4 || format == ORC_INT4;
   if (n > 0 && (!x || !codes || (need_scales && !scales))) return ORC_ERR_ARG;
 
   float alpha = 0.0f;
@@ -577,8 +614,8 @@ int orc_quantize(int format, int in_dtype, int granularity, int block_size, int 
 #pragma omp parallel for schedule(static) num_threads(nt)
 #endif
   for (int64_t r = 0; r < rows; ++r)
-    quantize_row(format, in_dtype, granularity, scale_round, r, cols, ld, x, codes, scales,
-                 tscale, acc ? &acc[r] : NULL);
+    quantize_row(format, in_dtype, granularity, scale_round, block_size, r, cols, ld, x, codes,
+                 scales, tscale, acc ? &acc[r] : NULL);
   if (stats_out) {
     finish_stats(stats_out, acc, rows, n);
     free(acc);
@@ -591,8 +628,12 @@ int orc_quantize(int format, int in_dtype, int granularity, int block_size, int 
 /* ------------------------------------------------------------------------------------ */
 
 /* x^ of element (r, c): decode(q) * s, s as in quantize */
-static float dequant_elem(int format, int granularity, int64_t r, int64_t c, int64_t cols,
-                          const void* codes, const void* scales, float tscale) {
+static float dequant_elem(int format, int granularity, int block_size, int64_t r, int64_t c,
+                          int64_t cols, const void* codes, const void* scales, float tscale) {
+  if (format == ORC_INT4) {
+    const float s = get_f32(scales, r * (cols / block_size) + c / block_size);
+    return (float)dec_int4(get_nibble(codes, r * (cols / 2), c)) * s;
+  }
   if (is8bit(format)) {
     float s = 1.0f;
     if (granularity == ORC_GRAN_ROW) s = get_f32(scales, r);
@@ -618,8 +659,8 @@ int orc_dequantize(int format, int granularity, int block_size, int64_t rows, in
   if (out_dtype != ORC_BF16 && out_dtype != ORC_F32) return ORC_ERR_ARG;
   const int64_t n = rows * cols;
   if (n == 0) return ORC_OK;
-  const int need_scales =
-      (granularity == ORC_GRAN_ROW) || format == ORC_MXFP4 || format == ORC_NVFP4;
+  const int need_scales = (granularity == ORC_GRAN_ROW) || format == ORC_MXFP4 ||
+                          format == ORC_NVFP4 || format == ORC_INT4;
   const int need_ts = (is8bit(format) && granularity == ORC_GRAN_TENSOR) ||
                       (format == ORC_NVFP4 && granularity == ORC_GRAN_BLOCK);
   if (!codes || !y || (need_scales && !scales) || (need_ts && !tensor_scale))
@@ -632,7 +673,7 @@ int orc_dequantize(int format, int granularity, int block_size, int64_t rows, in
   for (int64_t r = 0; r < rows; ++r)
     for (int64_t c = 0; c < cols; ++c)
       store_y(y, out_dtype, r * ld + c,
-              dequant_elem(format, granularity, r, c, cols, codes, scales, ts));
+              dequant_elem(format, granularity, block_size, r, c, cols, codes, scales, ts));
   (void)nt;
   return ORC_OK;
 }
@@ -646,8 +687,8 @@ int orc_error_stats(int format, int in_dtype, int granularity, int block_size, i
   if (check_shape(format, granularity, block_size, rows, cols, ld)) return ORC_ERR_ARG;
   if (in_dtype != ORC_BF16 && in_dtype != ORC_F32) return ORC_ERR_ARG;
   const int64_t n = rows * cols;
-  const int need_scales =
-      (granularity == ORC_GRAN_ROW) || format == ORC_MXFP4 || format == ORC_NVFP4;
+  const int need_scales = (granularity == ORC_GRAN_ROW) || format == ORC_MXFP4 ||
+                          format == ORC_NVFP4 || format == ORC_INT4;
   const int need_ts = (is8bit(format) && granularity == ORC_GRAN_TENSOR) ||
                       (format == ORC_NVFP4 && granularity == ORC_GRAN_BLOCK);
   if (n > 0 && (!x || !codes || (need_scales && !scales) || (need_ts && !tensor_scale)))
@@ -665,8 +706,42 @@ int orc_error_stats(int format, int in_dtype, int granularity, int block_size, i
   for (int64_t r = 0; r < rows; ++r)
     for (int64_t c = 0; c < cols; ++c)
       acc_elem(&acc[r], load_x(x, in_dtype, r * ld + c),
-               dequant_elem(format, granularity, r, c, cols, codes, scales, ts));
+               dequant_elem(format, granularity, block_size, r, c, cols, codes, scales, ts));
   finish_stats(stats_out, acc, rows, n);
   free(acc);
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* asymmetric 4-bit group dequantization ("Puzzles 12 Quantized Matrix Mult")             */
+/* ------------------------------------------------------------------------------------ */
+
+/* nibble i of a 32-bit word, low nibble first */
+static uint32_t word_nibble(const uint32_t* words, int64_t i) {
+  return (words[i / 8] >> (4 * (i % 8))) & 0xFu;
+}
+
+int orc_dequant_asym4(int64_t rows, int64_t cols, int64_t group, const uint32_t* w,
+                      const float* scales, const uint32_t* shifts, void* y, int out_dtype,
+                      int nthreads) {
+  if (rows < 0 || cols < 0 || group <= 0 || cols % 8 || cols % group) return ORC_ERR_ARG;
+  if (out_dtype != ORC_BF16 && out_dtype != ORC_F32) return ORC_ERR_ARG;
+  if (rows * cols == 0) return ORC_OK;
+  if (!w || !scales || !shifts || !y) return ORC_ERR_ARG;
+  const int64_t ng = cols / group, sw = (ng + 7) / 8;
+  const int nt = nthreads_of(nthreads);
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(nt)
+#endif
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int64_t c = 0; c < cols; ++c) {
+      const int64_t j = c / group;
+      const int q = (int)word_nibble(w + r * (cols / 8), c);
+      const int sh = (int)word_nibble(shifts + r * sw, j);
+      const float d = (float)(q - sh); /* exact: |q - sh| <= 15 */
+      store_y(y, out_dtype, r * cols + c, get_f32(scales, r * ng + j) * d);
+    }
+  }
+  (void)nt;
   return ORC_OK;
 }

@@ -33,6 +33,7 @@ extern "C" {
 #define ORC_E5M2 3
 #define ORC_MXFP4 4
 #define ORC_NVFP4 5
+#define ORC_INT4 6 /* symmetric, q in [-7, 7], fp32 scale per group of block_size */
 /* element formats only used by the table helpers */
 #define ORC_E2M1 16
 #define ORC_E8M0 17
@@ -69,7 +70,7 @@ double orc_decode_fp32(uint32_t bits);
 double orc_decode_bf16(uint16_t bits);
 uint32_t orc_encode_fp32(double v);          /* v must be exactly representable in binary32 */
 uint16_t orc_bf16_rne(uint32_t fp32_bits);   /* binary32 -> bf16, round to nearest even     */
-double orc_decode_code(int fmt, uint32_t code);   /* ORC_INT8 / E4M3 / E5M2 / E2M1 / E8M0  */
+double orc_decode_code(int fmt, uint32_t code);   /* ORC_INT8 / INT4 / E4M3 / E5M2 / E2M1 / E8M0 */
 uint32_t orc_encode_elem(int fmt, uint32_t v_fp32_bits); /* RNE, saturating, signed zero   */
 int orc_mx_scale_exponent(uint32_t t_fp32_bits, int scale_round); /* k of s = 2^k          */
 uint32_t orc_nv_block_scale_code(uint32_t t_fp32_bits, int scale_round); /* E4M3 code      */
@@ -92,6 +93,19 @@ int orc_error_stats(int format, int in_dtype, int granularity, int block_size,
                     int64_t rows, int64_t cols, int64_t ld, const void* x, const void* codes,
                     const void* scales, const float* tensor_scale, orc_stats* stats_out,
                     int nthreads);
+
+/* Asymmetric 4-bit group dequantization (section "Puzzles 12 Quantized Matrix Mult" of the
+ * blog's Triton post): y[r][c] = sc[r][c/group] * (w[r][c] - sh[r][c/group]).
+ *   w       [rows, cols/8] 32-bit words, 8 unsigned 4-bit codes each, element c in bits
+ *           [4*(c%8), 4*(c%8)+4) of word c/8 (the puzzle's extract: low nibble first)
+ *   scales  [rows, cols/group] fp32
+ *   shifts  [rows, ceil((cols/group)/8)] 32-bit words, 8 unsigned 4-bit shifts each, the
+ *           same nibble order
+ * cols % 8 == 0, group > 0, cols % group == 0.  w - sh is an exact small integer; the
+ * product is one binary32 rounding, then y is written as bf16 (RNE) or fp32. */
+int orc_dequant_asym4(int64_t rows, int64_t cols, int64_t group, const uint32_t* w,
+                      const float* scales, const uint32_t* shifts, void* y, int out_dtype,
+                      int nthreads);
 
 #ifdef __cplusplus
 }

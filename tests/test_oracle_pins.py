@@ -512,3 +512,109 @@ def test_empty(orc):
     x = np.zeros((0, 32), dtype=np.float32)
     codes, sc, ts, st = orc.quantize(x, orc.NVFP4, orc.GRAN_BLOCK, stats=True)
     assert codes.size == 0 and st.n == 0 and st.mse == 0 and ts == 1.0
+
+
+# ---------------------------------------------------------------- INT4 (symmetric, grouped)
+def test_int4_code_table(orc):
+    """4-bit two's complement nibbles; symmetric quantization never produces -8."""
+    g = golden("int4_facts.json")
+    vals = [orc.decode_code(orc.INT4, c) for c in range(16)]
+    assert vals == [float(v) for v in list(range(0, 8)) + list(range(-8, 0))]
+    for q in range(g["qmin"], g["qmax"] + 1):
+        assert orc.encode_elem(orc.INT4, float(q)) == (q & 0xF)
+    assert orc.encode_elem(orc.INT4, -100.0) == (g["qmin"] & 0xF)   # saturates at -7, not -8
+    assert orc.encode_elem(orc.INT4, 100.0) == g["qmax"]
+
+
+def test_int4_rounding_brute_force(orc):
+    """Element codes are round-half-to-even of v, clamped to [-7, 7] (numpy's rint)."""
+    rng = np.random.default_rng(41)
+    v = np.concatenate([rng.uniform(-9, 9, 4000), np.arange(-9, 9.5, 0.5)]).astype(np.float32)
+    for x in v:
+        q = int(np.clip(np.rint(np.float64(x)), -7, 7))
+        assert orc.encode_elem(orc.INT4, float(x)) == (q & 0xF), x
+
+
+@pytest.mark.parametrize("bs", [16, 32, 64, 128])
+def test_int4_scale_bound_and_zero_threshold(orc, bs):
+    """s = A/7 per group: the group's largest element maps to +-7, |e| <= s/2 = A/14, and
+    |x| below the zero threshold A/14 (= s/2; the tie itself goes to the even 0) gives 0."""
+    g = golden("int4_facts.json")
+    assert abs(g["zero_threshold_fraction_of_A"] - 1 / g["abs_error_divisor"]) < 5e-5
+    rng = np.random.default_rng(40 + bs)
+    x = (rng.standard_normal((8, 4 * bs)) * np.exp(rng.uniform(-3, 3, (8, 1)))).astype(np.float32)
+    codes, scales, _, st = orc.quantize(x, orc.INT4, orc.GRAN_BLOCK, stats=True, block_size=bs)
+    assert scales.shape == (8, 4) and scales.dtype == np.float32
+    q = (codes[:, :, None] >> np.array([0, 4], dtype=np.uint8)) & 0xF
+    q = q.reshape(8, 4 * bs).astype(np.int64)
+    q = np.where(q >= 8, q - 16, q)
+    assert q.min() >= g["qmin"] and q.max() <= g["qmax"]
+    xg = x.reshape(8, 4, bs).astype(np.float64)
+    A = np.abs(xg).max(axis=2)
+    assert np.array_equal(scales, (A.astype(np.float32) / np.float32(g["scale_divisor"])))
+    qg = q.reshape(8, 4, bs)
+    top = np.abs(xg).argmax(axis=2)
+    assert np.all(np.abs(np.take_along_axis(qg, top[..., None], 2)) == g["qmax"])
+    err = np.abs(xg - qg * scales[..., None].astype(np.float64))
+    assert np.all(err <= A[..., None] / g["abs_error_divisor"] * (1 + 2 ** -20))
+    s = scales[..., None].astype(np.float64)
+    zero = np.abs(xg) < s / 2
+    assert np.all(qg[zero] == 0)
+    assert np.all(qg[np.abs(xg) > s / 2 * (1 + 2 ** -20)] != 0)
+    # the tie x = s/2 rounds to the even integer 0; 3s/2 to 2
+    xt = np.zeros((1, bs), dtype=np.float32)
+    xt[0, 0], xt[0, 1], xt[0, 2] = 7.0, 0.5, 1.5
+    ct, st_, _, _ = orc.quantize(xt, orc.INT4, orc.GRAN_BLOCK, block_size=bs)
+    assert st_[0, 0] == 1.0 and ct[0, 0] == 0x07 and ct[0, 1] == 0x02
+
+
+def test_int4_zero_group_and_dequantize(orc):
+    x = np.zeros((2, 64), dtype=np.float32)
+    x[1, 32:] = np.linspace(-3, 3, 32, dtype=np.float32)
+    codes, scales, ts, st = orc.quantize(x, orc.INT4, orc.GRAN_BLOCK, stats=True)
+    assert scales[0, 0] == 1.0 and not codes[0].any()              # A = 0: s := 1, codes 0
+    y = orc.dequantize(codes, scales, ts, orc.INT4, orc.GRAN_BLOCK, 2, 64, out_dtype=orc.F32)
+    nib = np.stack([codes & 0xF, codes >> 4], axis=-1).reshape(2, 64).astype(np.int64)
+    nib = np.where(nib >= 8, nib - 16, nib)
+    s = np.repeat(scales, 32, axis=1)
+    assert np.array_equal(y, (nib.astype(np.float32) * s).astype(np.float32))
+    st2 = orc.error_stats(x, codes, scales, ts, orc.INT4, orc.GRAN_BLOCK)
+    assert st2 == st
+
+
+# ---------------------------------------------------------------- Puzzle 12: asymmetric 4-bit
+def test_asym4_worked_example(orc):
+    g = golden("puzzle12_asym_dequant.json")
+    ex = g["example"]
+    w = np.array([ex["w_words"]], dtype=np.uint32)
+    y = orc.dequant_asym4(w, np.array([[ex["scale"]]], dtype=np.float32),
+                          np.array([[ex["shift"]]], dtype=np.uint32), 1, 16, ex["group"])
+    assert y[0].tolist() == ex["y"]
+
+
+def test_asym4_identity_order_and_groups(orc):
+    """sc = 1, sh = 0 returns the packed codes themselves, in the puzzle's nibble order; each
+    element uses the scale and shift of group c // group (shifts packed 8 per word)."""
+    g = golden("nibble_order.json")
+    assert g["first_element"] == "low nibble"
+    rng = np.random.default_rng(44)
+    rows, cols, group = 3, 256, 16
+    codes = rng.integers(0, 16, (rows, cols))
+    w = np.zeros((rows, cols // 8), dtype=np.uint32)
+    for j in range(8):
+        w |= (codes[:, j::8].astype(np.uint32) << np.uint32(4 * j))
+    ng = cols // group
+    y = orc.dequant_asym4(w, np.ones((rows, ng), np.float32), np.zeros((rows, 2), np.uint32),
+                          rows, cols, group)
+    assert np.array_equal(y, codes.astype(np.float32))
+    # per-group powers of two and shifts: exact, so every element is checkable by hand
+    sc = (2.0 ** rng.integers(-4, 5, (rows, ng))).astype(np.float32)
+    shv = rng.integers(0, 16, (rows, ng))
+    sh = np.zeros((rows, 2), dtype=np.uint32)
+    for j in range(ng):
+        sh[:, j // 8] |= shv[:, j].astype(np.uint32) << np.uint32(4 * (j % 8))
+    y = orc.dequant_asym4(w, sc, sh, rows, cols, group)
+    gi = np.arange(cols) // group
+    assert np.array_equal(y, (sc[:, gi] * (codes - shv[:, gi])).astype(np.float32))
+    yb = orc.dequant_asym4(w, sc, sh, rows, cols, group, out_dtype=orc.BF16)
+    assert np.array_equal(yb, (y.view(np.uint32) >> 16).astype(np.uint16))  # exact in bf16
