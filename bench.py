@@ -159,9 +159,11 @@ class ClockSampler:
 # tensor's own, computed beforehand) and this tensor's amax returned, in one pass.
 MATRIX = [
     (1, None, [("int8", "tensor"), ("e4m3", "tensor"), ("mxfp4", "block"), ("nvfp4", "block")]),
-    (2, None, [("int8", "row"), ("e4m3", "row"), ("mxfp4", "block"), ("nvfp4", "block")]),
+    (2, None, [("int8", "row"), ("e4m3", "row"), ("mxfp4", "block"), ("nvfp4", "block"),
+               ("int4", "block", 128), ("asym4", "group", 128)]),
     (3, None, [("e4m3", "row"), ("e5m2", "row"), ("nvfp4", "block"), ("nvfp4", "block", "delayed")]),
-    (4, None, [("mxfp4", "block"), ("nvfp4", "block"), ("nvfp4", "block", "delayed")]),
+    (4, None, [("mxfp4", "block"), ("nvfp4", "block"), ("nvfp4", "block", "delayed"),
+               ("int4", "block", 32)]),
     (5, 4096, [(f, g) for f in ("int8", "e4m3", "e5m2") for g in ("unit", "tensor")] +
               [(f, g) for f in ("mxfp4", "nvfp4") for g in ("unit", "block")] +
               [("e4m3", "tensor", "delayed"), ("nvfp4", "block", "delayed")]),
@@ -214,11 +216,15 @@ def measure_matrix(dev, peaks, flush, x4=None, reps=10, which=(1, 2, 3, 4, 5)) -
         a_out = torch.empty((1,), dtype=torch.float32, device=dev)
         for run in runs:
             fname, gname = run[0], run[1]
-            delayed = len(run) > 2
+            if fname == "asym4":
+                out.append(measure_asym4(name, r, c, run[2], timed, peaks, dev))
+                continue
+            delayed = len(run) > 2 and run[2] == "delayed"
+            bsz = run[2] if len(run) > 2 and isinstance(run[2], int) else None
             f, g = qz.FORMATS[fname], qz.GRANULARITIES[gname]
-            codes, scales, ts = qz.alloc_outputs(f, g, r, c, dev)
+            codes, scales, ts = qz.alloc_outputs(f, g, r, c, dev, bsz)
             y = torch.empty((r, c), dtype=x.dtype, device=dev)
-            d = qz.make_desc(f, idt, g, r, c)
+            d = qz.make_desc(f, idt, g, r, c, block_size=bsz)
             amax_pass = not delayed and (g == qz.QZ_GRAN_TENSOR or
                                          (f == qz.QZ_NVFP4 and g == qz.QZ_GRAN_BLOCK))
 
@@ -241,7 +247,8 @@ def measure_matrix(dev, peaks, flush, x4=None, reps=10, which=(1, 2, 3, 4, 5)) -
             qb = n * eb * (2 if amax_pass else 1) + cb + 32 + (8 if delayed else 0)
             db = cb + n * eb
             out.append({"workload": name, "format": fname,
-                        "granularity": gname + (" delayed" if delayed else ""),
+                        "granularity": gname + (" delayed" if delayed else "") +
+                                       (f" {bsz}" if bsz else ""),
                         "quantize_us": round(qms * 1e3, 1),
                         "quantize_gbs": round(qb / qms / 1e6, 1),
                         "quantize_frac": round(qb / qms / 1e6 / peaks["hbm_gbs"], 3),
@@ -253,6 +260,34 @@ def measure_matrix(dev, peaks, flush, x4=None, reps=10, which=(1, 2, 3, 4, 5)) -
     if ws.status() != 0:
         raise RuntimeError("status flags set during the format matrix")
     return out
+
+
+def measure_asym4(name, rows, cols, group, timed, peaks, dev) -> dict:
+    """The asymmetric 4-bit group dequantization on a weight of the workload's shape: seeded
+    random codes, shifts and scales made on the device (not timed), bf16 output."""
+    import torch
+    import precision_quantization_gb300 as qz
+    gen = torch.Generator(device=dev).manual_seed(7)
+    w = torch.randint(-2 ** 31, 2 ** 31 - 1, (rows, cols // 8), dtype=torch.int32, device=dev,
+                      generator=gen)
+    ng = cols // group
+    sc = torch.randn((rows, ng), dtype=torch.float32, device=dev, generator=gen)
+    sh = torch.randint(-2 ** 31, 2 ** 31 - 1, (rows, (ng + 7) // 8), dtype=torch.int32,
+                       device=dev, generator=gen)
+    y = torch.empty((rows, cols), dtype=torch.bfloat16, device=dev)
+    sp = torch.cuda.current_stream(dev).cuda_stream
+
+    def dq():
+        rc = qz.qz_dequantize_asym4(w.data_ptr(), sc.data_ptr(), sh.data_ptr(), rows, cols, group,
+                                    y.data_ptr(), cols, qz.QZ_BF16, sp)
+        assert rc == 0, rc
+    dms = timed(dq)
+    db = w.numel() * 4 + sc.numel() * 4 + sh.numel() * 4 + y.numel() * 2
+    return {"workload": name, "format": "asym4", "granularity": f"group {group}",
+            "quantize_us": None, "quantize_gbs": None, "quantize_frac": None,
+            "quantize_launches": 0,
+            "dequantize_us": round(dms * 1e3, 1), "dequantize_gbs": round(db / dms / 1e6, 1),
+            "dequantize_frac": round(db / dms / 1e6 / peaks["hbm_gbs"], 3)}
 
 
 def dist_setup():

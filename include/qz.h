@@ -1,6 +1,7 @@
 /*
  * qz.h -- C ABI of libqz: quantize a 2-D tensor on a GB300 (sm_103a) GPU to symmetric INT8,
- * FP8 E4M3 / E5M2, MXFP4 or NVFP4, dequantize it again, and reduce the quantization error.
+ * FP8 E4M3 / E5M2, MXFP4, NVFP4 or grouped symmetric INT4, dequantize it again, and reduce
+ * the quantization error; dequantize asymmetric 4-bit grouped weights.
  *
  * The operations are the ones defined in the blog post "浅谈低精度浮点数" ("A brief talk
  * on low-precision floats", july-h5kf3.github.io column blog):
@@ -11,7 +12,11 @@
  *     up in practice), NVFP4 (16 values share one E4M3 scale, times one fp32 per-tensor
  *     scale: s_global = global_amax / (6 * 448), s_block = (block_amax / 6) / s_global,
  *     x^ = s_global * s_block * Q_E2M1(x / (s_global * s_block)));
+ *   - same section, closing paragraph: symmetric INT4, q in [-7, 7], s = A / 7, analysed
+ *     like INT8 (here one fp32 scale per group of block_size values along cols);
  *   - the error measures discussed there: |x - x^| and |x - x^| / |x|.
+ * The asymmetric 4-bit group dequantization sc * (w - sh) is the one of the "Puzzles 12
+ * Quantized Matrix Mult" section of the same blog's "Triton" post.
  * Packing of two FP4 codes per byte follows the "Puzzles 12 Quantized Matrix Mult" section
  * of the same blog's "Triton" post: element j of a packed word sits in bits [4j, 4j+4), so
  * the first element of a pair is the low nibble.
@@ -34,6 +39,9 @@
  *                  saturated at 448 (QZ_SCALE_UP) or RNE-saturating E4M3 (QZ_SCALE_NEAREST);
  *                  s = fl32(s_g * decode(block code)); s = 0 gives signed-zero codes.
  *                  UNIT uses s_g = 1 and block code 0x38 (1.0).
+ *   INT4           per group of block_size values with largest magnitude A: s = fl32(A / 7)
+ *                  (1 when 0), q = RNE(fl32(x / s)) clamped to [-7, 7], one zero; stored as
+ *                  a 4-bit two's complement nibble (-8 never occurs).
  *   dequantize     x^ = fl32(decode(q) * s), then converted to the output dtype (bf16 by
  *                  round-to-nearest-even, or fp32 as is).
  *   stats          e = fl32(x - x^) with the fp32 x^; sum_sq_err = sum e^2; mse =
@@ -45,11 +53,12 @@
  * Layouts.  The high-precision tensor (x for quantize / stats, y for dequantize) is
  * [rows, cols] row-major with leading dimension ld >= cols, in elements.  Everything else
  * is dense row-major:
- *   codes   INT8 / FP8: rows * cols bytes; MXFP4 / NVFP4: rows * cols / 2 bytes.
+ *   codes   INT8 / FP8: rows * cols bytes; MXFP4 / NVFP4 / INT4: rows * cols / 2 bytes.
  *   scales  ROW: rows fp32; MXFP4: rows * cols / 32 E8M0 bytes; NVFP4: rows * cols / 16
- *           E4M3 bytes; otherwise unused (may be NULL).
+ *           E4M3 bytes; INT4: rows * cols / block_size fp32; otherwise unused (may be NULL).
  *   tensor_scale  one fp32: s for TENSOR, s_g for NVFP4 BLOCK, 1 for UNIT.
- * Blocks run along cols.  MXFP4 needs cols % 32 == 0, NVFP4 cols % 16 == 0.
+ * Blocks run along cols.  MXFP4 needs cols % 32 == 0, NVFP4 cols % 16 == 0, INT4
+ * cols % block_size == 0.
  *
  * Ownership and concurrency.  The caller allocates every buffer (all device memory except
  * the host pointer of qz_get_device_status).  The library allocates nothing; its only
@@ -97,12 +106,14 @@ typedef enum {
   QZ_ERR_WORKSPACE = 7    /* workspace missing or smaller than qz_workspace_size()     */
 } qz_status;
 
-typedef enum { QZ_INT8 = 1, QZ_FP8_E4M3 = 2, QZ_FP8_E5M2 = 3, QZ_MXFP4 = 4, QZ_NVFP4 = 5 } qz_format;
+typedef enum {
+  QZ_INT8 = 1, QZ_FP8_E4M3 = 2, QZ_FP8_E5M2 = 3, QZ_MXFP4 = 4, QZ_NVFP4 = 5, QZ_INT4 = 6
+} qz_format;
 typedef enum { QZ_BF16 = 1, QZ_F32 = 2 } qz_dtype;
 typedef enum {
   QZ_GRAN_TENSOR = 1, /* one scale for the tensor (INT8 / FP8)                     */
   QZ_GRAN_ROW = 2,    /* one scale per row: per output channel / per token (INT8/FP8) */
-  QZ_GRAN_BLOCK = 3,  /* per block along cols (MXFP4 32, NVFP4 16)                 */
+  QZ_GRAN_BLOCK = 3,  /* per block along cols (MXFP4 32, NVFP4 16, INT4 block_size) */
   QZ_GRAN_UNIT = 4    /* scale 1: the bare element cast (all formats)              */
 } qz_granularity;
 typedef enum { QZ_ROUND_RNE = 0 } qz_elem_round;
@@ -118,7 +129,7 @@ typedef struct {
   int32_t format;      /* qz_format                                                  */
   int32_t in_dtype;    /* qz_dtype of x (quantize, stats, amax)                      */
   int32_t granularity; /* qz_granularity                                             */
-  int32_t block_size;  /* 32 for MXFP4, 16 for NVFP4, 0 for INT8 / FP8               */
+  int32_t block_size;  /* 32 for MXFP4, 16 for NVFP4, 16/32/64/128 for INT4, else 0  */
   int32_t elem_round;  /* QZ_ROUND_RNE                                               */
   int32_t scale_round; /* qz_scale_round (MXFP4 / NVFP4 BLOCK)                       */
   int64_t rows;        /* >= 0                                                       */
@@ -214,6 +225,21 @@ QZ_API qz_status qz_error_stats(const qz_desc* desc, const void* x, const void* 
 QZ_API qz_status qz_error_stats_noalloc(const qz_desc* desc, const void* x, const void* codes,
                                         const void* scales, const float* tensor_scale_dev,
                                         qz_stats* stats_dev, qz_stream_t stream);
+
+/* Asymmetric 4-bit group dequantization ("Puzzles 12 Quantized Matrix Mult", Triton post):
+ *   y[r][c] = fl32(sc[r][c / group] * (w[r][c] - sh[r][c / group])), w - sh exact.
+ *   w       device, [rows, cols / 8] 32-bit words: 8 unsigned 4-bit codes each, element c
+ *           in bits [4 (c % 8), 4 (c % 8) + 4) of word c / 8 (the puzzle's extract order)
+ *   scales  device, [rows, cols / group] fp32
+ *   shifts  device, [rows, ceil((cols / group) / 8)] 32-bit words: 8 unsigned 4-bit shifts
+ *           each, group j in nibble j % 8 of word j / 8
+ *   y       device, [rows, ld] of out_dtype (bf16 by RNE, or fp32), ld >= cols
+ * Requires cols % 8 == 0, group > 0, cols % group == 0 (QZ_ERR_SHAPE otherwise); words and
+ * scales 4-byte aligned.  Asynchronous on `stream`; needs no workspace. */
+QZ_API qz_status qz_dequantize_asym4(const uint32_t* w, const float* scales,
+                                     const uint32_t* shifts, int64_t rows, int64_t cols,
+                                     int64_t group, void* y, int64_t ld, int32_t out_dtype,
+                                     qz_stream_t stream);
 
 /* Synchronize `stream`, then copy the workspace status word (QZ_FLAG_* bits, sticky until
  * qz_workspace_init) into *flags_host. */

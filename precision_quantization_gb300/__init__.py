@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(_HERE, "libqz.so")
 # ---- enums (values of include/qz.h) ----
 QZ_OK, QZ_ERR_NULL, QZ_ERR_ENUM, QZ_ERR_SHAPE, QZ_ERR_ALIGN = 0, 1, 2, 3, 4
 QZ_ERR_UNSUPPORTED, QZ_ERR_CUDA, QZ_ERR_WORKSPACE = 5, 6, 7
-QZ_INT8, QZ_FP8_E4M3, QZ_FP8_E5M2, QZ_MXFP4, QZ_NVFP4 = 1, 2, 3, 4, 5
+QZ_INT8, QZ_FP8_E4M3, QZ_FP8_E5M2, QZ_MXFP4, QZ_NVFP4, QZ_INT4 = 1, 2, 3, 4, 5, 6
 QZ_BF16, QZ_F32 = 1, 2
 QZ_GRAN_TENSOR, QZ_GRAN_ROW, QZ_GRAN_BLOCK, QZ_GRAN_UNIT = 1, 2, 3, 4
 QZ_ROUND_RNE = 0
@@ -31,15 +31,15 @@ QZ_SCALE_UP, QZ_SCALE_NEAREST = 0, 1
 QZ_FLAG_NONFINITE_INPUT, QZ_FLAG_BAD_AMAX, QZ_FLAG_PIPELINE_TIMEOUT = 0x1, 0x2, 0x4
 
 FORMATS = {"int8": QZ_INT8, "e4m3": QZ_FP8_E4M3, "e5m2": QZ_FP8_E5M2,
-           "mxfp4": QZ_MXFP4, "nvfp4": QZ_NVFP4}
+           "mxfp4": QZ_MXFP4, "nvfp4": QZ_NVFP4, "int4": QZ_INT4}
 GRANULARITIES = {"tensor": QZ_GRAN_TENSOR, "row": QZ_GRAN_ROW, "block": QZ_GRAN_BLOCK,
                  "unit": QZ_GRAN_UNIT}
-BLOCK_SIZE = {QZ_MXFP4: 32, QZ_NVFP4: 16}
+BLOCK_SIZE = {QZ_MXFP4: 32, QZ_NVFP4: 16, QZ_INT4: 32}  # INT4: the default group
 
 # Names of the exported C symbols (the whole ABI of include/qz.h).
 ABI_SYMBOLS = ("qz_status_string", "qz_workspace_size", "qz_workspace_init", "qz_amax",
                "qz_quantize", "qz_quantize_delayed", "qz_dequantize", "qz_error_stats",
-               "qz_error_stats_noalloc", "qz_get_device_status")
+               "qz_error_stats_noalloc", "qz_dequantize_asym4", "qz_get_device_status")
 
 
 class QzDesc(C.Structure):
@@ -85,6 +85,8 @@ def lib():
             "qz_error_stats": (i32, [dp, vp, vp, vp, vp, vp, vp, vp]),
             "qz_error_stats_noalloc": (i32, [dp, vp, vp, vp, vp, vp, vp]),
             "qz_get_device_status": (i32, [vp, C.POINTER(C.c_uint32), vp]),
+            "qz_dequantize_asym4": (i32, [vp, vp, vp, C.c_int64, C.c_int64, C.c_int64, vp,
+                                          C.c_int64, i32, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -122,6 +124,12 @@ def qz_quantize_delayed(desc: QzDesc, x: int, codes: int, scales: int | None,
                         stats_dev: int | None, ws: int, stream: int = 0) -> int:
     return lib().qz_quantize_delayed(C.byref(desc), x, codes, scales, tensor_scale_dev,
                                      amax_in_dev, amax_out_dev, stats_dev, ws, stream)
+
+
+def qz_dequantize_asym4(w: int, scales: int, shifts: int, rows: int, cols: int, group: int,
+                        y: int, ld: int, out_dtype: int, stream: int = 0) -> int:
+    return lib().qz_dequantize_asym4(w, scales, shifts, rows, cols, group, y, ld, out_dtype,
+                                     stream)
 
 
 def qz_dequantize(desc: QzDesc, codes: int, scales: int | None, tensor_scale_dev: int | None,
@@ -171,7 +179,7 @@ def _gran(g) -> int:
 
 
 def default_granularity(fmt: int) -> int:
-    return QZ_GRAN_BLOCK if fmt in (QZ_MXFP4, QZ_NVFP4) else QZ_GRAN_TENSOR
+    return QZ_GRAN_BLOCK if fmt in (QZ_MXFP4, QZ_NVFP4, QZ_INT4) else QZ_GRAN_TENSOR
 
 
 def _dtype_code(dt) -> int:
@@ -184,9 +192,11 @@ def _dtype_code(dt) -> int:
 
 
 def make_desc(fmt, in_dtype: int, granularity, rows: int, cols: int, ld: int | None = None,
-              scale_round: int = QZ_SCALE_UP) -> QzDesc:
+              scale_round: int = QZ_SCALE_UP, block_size: int | None = None) -> QzDesc:
+    """block_size: the INT4 group (16, 32, 64, 128; default 32); fixed by the format else."""
     f = _fmt(fmt)
-    return QzDesc(f, in_dtype, _gran(granularity), BLOCK_SIZE.get(f, 0), QZ_ROUND_RNE,
+    bs = block_size if (f == QZ_INT4 and block_size is not None) else BLOCK_SIZE.get(f, 0)
+    return QzDesc(f, in_dtype, _gran(granularity), bs, QZ_ROUND_RNE,
                   scale_round, rows, cols, cols if ld is None else ld)
 
 
@@ -234,13 +244,15 @@ class Workspace:
 @dataclass
 class Quantized:
     codes: object          # uint8 [rows, cols] or [rows, cols/2]
-    scales: object         # fp32 [rows] (ROW), uint8 [rows, cols/bs] (FP4), or None
+    scales: object         # fp32 [rows] (ROW), uint8 [rows, cols/bs] (FP4),
+                           # fp32 [rows, cols/bs] (INT4), or None
     tensor_scale: object   # fp32 [1]
     fmt: int
     granularity: int
     scale_round: int
     rows: int
     cols: int
+    block_size: int = 0    # the INT4 group (0: the format's own block)
 
 
 @dataclass
@@ -261,12 +273,14 @@ def read_stats(t) -> Stats:
     return stats_from_bytes(t.cpu().numpy().tobytes())
 
 
-def alloc_outputs(fmt: int, granularity: int, rows: int, cols: int, device):
+def alloc_outputs(fmt: int, granularity: int, rows: int, cols: int, device,
+                  block_size: int | None = None):
     torch = _torch()
-    bs = BLOCK_SIZE.get(fmt, 0)
+    bs = block_size if (fmt == QZ_INT4 and block_size is not None) else BLOCK_SIZE.get(fmt, 0)
     codes = torch.empty((rows, cols // 2 if bs else cols), dtype=torch.uint8, device=device)
     if bs:
-        scales = torch.empty((rows, cols // bs), dtype=torch.uint8, device=device)
+        scales = torch.empty((rows, cols // bs),
+                             dtype=torch.float32 if fmt == QZ_INT4 else torch.uint8, device=device)
     elif granularity == QZ_GRAN_ROW:
         scales = torch.empty((rows,), dtype=torch.float32, device=device)
     else:
@@ -276,7 +290,8 @@ def alloc_outputs(fmt: int, granularity: int, rows: int, cols: int, device):
 
 
 def quantize(x, fmt, granularity=None, scale_round: int = QZ_SCALE_UP, tensor_amax=None,
-             stats: bool = False, workspace: Workspace | None = None, out=None, stream=None):
+             stats: bool = False, workspace: Workspace | None = None, out=None, stream=None,
+             block_size: int | None = None):
     """Quantize a 2-D bf16 / fp32 CUDA tensor.  Returns (Quantized, stats tensor or None).
 
     tensor_amax: optional fp32 CUDA tensor [1] with alpha (per-tensor / NVFP4 global amax).
@@ -286,8 +301,9 @@ def quantize(x, fmt, granularity=None, scale_round: int = QZ_SCALE_UP, tensor_am
     f = _fmt(fmt)
     g = default_granularity(f) if granularity is None else _gran(granularity)
     rows, cols, ld = _rows_cols_ld(x)
-    desc = make_desc(f, _dtype_code(x.dtype), g, rows, cols, ld, scale_round)
-    codes, scales, tscale = out if out is not None else alloc_outputs(f, g, rows, cols, x.device)
+    desc = make_desc(f, _dtype_code(x.dtype), g, rows, cols, ld, scale_round, block_size)
+    codes, scales, tscale = out if out is not None else alloc_outputs(f, g, rows, cols, x.device,
+                                                                      desc.block_size)
     st = torch.empty((STATS_BYTES,), dtype=torch.uint8, device=x.device) if stats else None
     need_ws = stats or (tensor_amax is None and (g == QZ_GRAN_TENSOR or
                                                  (f == QZ_NVFP4 and g == QZ_GRAN_BLOCK)))
@@ -297,12 +313,12 @@ def quantize(x, fmt, granularity=None, scale_round: int = QZ_SCALE_UP, tensor_am
                      _ptr(tensor_amax), _ptr(st), workspace.ptr if workspace else None,
                      _stream(stream))
     _check(rc, "qz_quantize")
-    return Quantized(codes, scales, tscale, f, g, scale_round, rows, cols), st
+    return Quantized(codes, scales, tscale, f, g, scale_round, rows, cols, desc.block_size), st
 
 
 def quantize_delayed(x, fmt, amax_in, granularity=None, scale_round: int = QZ_SCALE_UP,
                      stats: bool = False, workspace: Workspace | None = None, out=None,
-                     amax_out=None, stream=None):
+                     amax_out=None, stream=None, block_size: int | None = None):
     """Quantize with the per-tensor scale of an earlier tensor's amax (amax_in: fp32 CUDA
     tensor [1], or None where the granularity needs none) and return this tensor's amax.
     Returns (Quantized, stats tensor or None, amax_out tensor [1])."""
@@ -310,8 +326,9 @@ def quantize_delayed(x, fmt, amax_in, granularity=None, scale_round: int = QZ_SC
     f = _fmt(fmt)
     g = default_granularity(f) if granularity is None else _gran(granularity)
     rows, cols, ld = _rows_cols_ld(x)
-    desc = make_desc(f, _dtype_code(x.dtype), g, rows, cols, ld, scale_round)
-    codes, scales, tscale = out if out is not None else alloc_outputs(f, g, rows, cols, x.device)
+    desc = make_desc(f, _dtype_code(x.dtype), g, rows, cols, ld, scale_round, block_size)
+    codes, scales, tscale = out if out is not None else alloc_outputs(f, g, rows, cols, x.device,
+                                                                      desc.block_size)
     st = torch.empty((STATS_BYTES,), dtype=torch.uint8, device=x.device) if stats else None
     workspace = workspace or Workspace(x.device)
     amax_out = amax_out if amax_out is not None else torch.empty((1,), dtype=torch.float32,
@@ -320,7 +337,8 @@ def quantize_delayed(x, fmt, amax_in, granularity=None, scale_round: int = QZ_SC
                              tscale.data_ptr(), _ptr(amax_in), amax_out.data_ptr(), _ptr(st),
                              workspace.ptr, _stream(stream))
     _check(rc, "qz_quantize_delayed")
-    return Quantized(codes, scales, tscale, f, g, scale_round, rows, cols), st, amax_out
+    return (Quantized(codes, scales, tscale, f, g, scale_round, rows, cols, desc.block_size), st,
+            amax_out)
 
 
 def dequantize(q: Quantized, out_dtype=None, out=None, stream=None):
@@ -330,10 +348,27 @@ def dequantize(q: Quantized, out_dtype=None, out=None, stream=None):
     y = out if out is not None else torch.empty((q.rows, q.cols), dtype=out_dtype,
                                                 device=q.codes.device)
     rows, cols, ld = _rows_cols_ld(y)
-    desc = make_desc(q.fmt, QZ_BF16, q.granularity, q.rows, q.cols, ld, q.scale_round)
+    desc = make_desc(q.fmt, QZ_BF16, q.granularity, q.rows, q.cols, ld, q.scale_round,
+                     q.block_size or None)
     rc = qz_dequantize(desc, q.codes.data_ptr(), _ptr(q.scales), _ptr(q.tensor_scale),
                        y.data_ptr(), _dtype_code(y.dtype), _stream(stream))
     _check(rc, "qz_dequantize")
+    return y
+
+
+def dequantize_asym4(w, scales, shifts, group: int, out_dtype=None, out=None, stream=None):
+    """Asymmetric 4-bit group dequantization y = sc * (w - sh) (see qz_dequantize_asym4):
+    w int32/uint32 CUDA tensor [rows, cols/8], scales fp32 [rows, cols/group], shifts
+    int32/uint32 [rows, ceil(cols/group/8)].  Returns a bf16 (default) or fp32 tensor."""
+    torch = _torch()
+    rows, wpr = w.shape
+    cols = wpr * 8
+    out_dtype = out_dtype or torch.bfloat16
+    y = out if out is not None else torch.empty((rows, cols), dtype=out_dtype, device=w.device)
+    _, _, ld = _rows_cols_ld(y)
+    rc = qz_dequantize_asym4(w.data_ptr(), scales.data_ptr(), shifts.data_ptr(), rows, cols,
+                             group, y.data_ptr(), ld, _dtype_code(y.dtype), _stream(stream))
+    _check(rc, "qz_dequantize_asym4")
     return y
 
 
@@ -341,7 +376,8 @@ def error_stats(x, q: Quantized, workspace: Workspace | None = None, stream=None
     """Error statistics of q against x: a device uint8[STATS_BYTES] qz_stats buffer."""
     torch = _torch()
     rows, cols, ld = _rows_cols_ld(x)
-    desc = make_desc(q.fmt, _dtype_code(x.dtype), q.granularity, rows, cols, ld, q.scale_round)
+    desc = make_desc(q.fmt, _dtype_code(x.dtype), q.granularity, rows, cols, ld, q.scale_round,
+                     q.block_size or None)
     st = torch.empty((STATS_BYTES,), dtype=torch.uint8, device=x.device)
     workspace = workspace or Workspace(x.device)
     rc = qz_error_stats(desc, x.data_ptr(), q.codes.data_ptr(), _ptr(q.scales),

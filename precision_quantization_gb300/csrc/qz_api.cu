@@ -118,6 +118,7 @@ __global__ void fill_kernel(float* a, float va, qz_stats* st, float* zero_out = 
 
 bool is8(int f) { return f == QZ_INT8 || f == QZ_FP8_E4M3 || f == QZ_FP8_E5M2; }
 bool is4(int f) { return f == QZ_MXFP4 || f == QZ_NVFP4; }
+bool isint4(int f) { return f == QZ_INT4; }
 bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
 
 qz_status check_shape(const qz_desc* d) {
@@ -131,7 +132,7 @@ qz_status check_dtype(int dt) { return (dt == QZ_BF16 || dt == QZ_F32) ? QZ_OK :
 // Format / granularity / block size / rounding fields.
 qz_status check_desc(const qz_desc* d) {
   if (!d) return QZ_ERR_NULL;
-  if (!is8(d->format) && !is4(d->format)) return QZ_ERR_ENUM;
+  if (!is8(d->format) && !is4(d->format) && !isint4(d->format)) return QZ_ERR_ENUM;
   if (d->granularity < QZ_GRAN_TENSOR || d->granularity > QZ_GRAN_UNIT) return QZ_ERR_ENUM;
   if (d->elem_round != QZ_ROUND_RNE) return QZ_ERR_ENUM;
   if (d->scale_round != QZ_SCALE_UP && d->scale_round != QZ_SCALE_NEAREST) return QZ_ERR_ENUM;
@@ -139,6 +140,11 @@ qz_status check_desc(const qz_desc* d) {
   if (st != QZ_OK) return st;
   if (is8(d->format)) {
     if (d->granularity == QZ_GRAN_BLOCK || d->block_size != 0) return QZ_ERR_UNSUPPORTED;
+  } else if (isint4(d->format)) {
+    const int bs = d->block_size;
+    if (bs != 16 && bs != 32 && bs != 64 && bs != 128) return QZ_ERR_UNSUPPORTED;
+    if (d->granularity != QZ_GRAN_BLOCK) return QZ_ERR_UNSUPPORTED;
+    if (d->cols % bs != 0) return QZ_ERR_SHAPE;
   } else {
     const int bs = d->format == QZ_MXFP4 ? 32 : 16;
     if (d->block_size != bs) return QZ_ERR_UNSUPPORTED;
@@ -148,7 +154,9 @@ qz_status check_desc(const qz_desc* d) {
   return QZ_OK;
 }
 
-bool needs_scales(const qz_desc* d) { return d->granularity == QZ_GRAN_ROW || is4(d->format); }
+bool needs_scales(const qz_desc* d) {
+  return d->granularity == QZ_GRAN_ROW || is4(d->format) || isint4(d->format);
+}
 bool needs_tscale(const qz_desc* d) {
   return (is8(d->format) && d->granularity == QZ_GRAN_TENSOR) ||
          (d->format == QZ_NVFP4 && d->granularity == QZ_GRAN_BLOCK);
@@ -236,7 +244,8 @@ extern "C" qz_status qz_quantize(const qz_desc* d, const void* x, void* codes, v
   if (needs_scales(d) && !scales) return QZ_ERR_NULL;
   const int eb = d->in_dtype == QZ_BF16 ? 2 : 4;
   if (!aligned(x, eb)) return QZ_ERR_ALIGN;
-  if (d->granularity == QZ_GRAN_ROW && !aligned(scales, 4)) return QZ_ERR_ALIGN;
+  if ((d->granularity == QZ_GRAN_ROW || isint4(d->format)) && !aligned(scales, 4)) return QZ_ERR_ALIGN;
+  if (isint4(d->format)) return launch_quant_int4(*d, x, codes, scales, tensor_scale_dev, stats_dev, ws, s);
   const float* amax = tensor_amax_dev;
   if (compute_amax) {
     if ((st = launch_amax(*d, x, nullptr, ws, s)) != QZ_OK) return st;
@@ -270,7 +279,11 @@ extern "C" qz_status qz_quantize_delayed(const qz_desc* d, const void* x, void* 
   if (needs_scales(d) && !scales) return QZ_ERR_NULL;
   const int eb = d->in_dtype == QZ_BF16 ? 2 : 4;
   if (!aligned(x, eb)) return QZ_ERR_ALIGN;
-  if (d->granularity == QZ_GRAN_ROW && !aligned(scales, 4)) return QZ_ERR_ALIGN;
+  if ((d->granularity == QZ_GRAN_ROW || isint4(d->format)) && !aligned(scales, 4)) return QZ_ERR_ALIGN;
+  if (isint4(d->format)) {
+    st = launch_quant_int4(*d, x, codes, scales, tensor_scale_dev, stats_dev, ws, s);
+    return st == QZ_OK ? launch_amax(*d, x, amax_out_dev, ws, s) : st;
+  }
   const float* amax = tensor_alpha ? amax_in_dev : nullptr;
   if (is8(d->format))
     return launch_quant8(*d, x, codes, scales, tensor_scale_dev, amax, true, stats_dev, ws, s, amax_out_dev);
@@ -288,9 +301,10 @@ extern "C" qz_status qz_dequantize(const qz_desc* d, const void* codes, const vo
   if (needs_scales(d) && !scales) return QZ_ERR_NULL;
   if (needs_tscale(d) && !tensor_scale_dev) return QZ_ERR_NULL;
   if (!aligned(y, out_dtype == QZ_BF16 ? 2 : 4)) return QZ_ERR_ALIGN;
-  if (d->granularity == QZ_GRAN_ROW && !aligned(scales, 4)) return QZ_ERR_ALIGN;
+  if ((d->granularity == QZ_GRAN_ROW || isint4(d->format)) && !aligned(scales, 4)) return QZ_ERR_ALIGN;
   if (tensor_scale_dev && !aligned(tensor_scale_dev, 4)) return QZ_ERR_ALIGN;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (isint4(d->format)) return launch_dequant_int4(*d, codes, scales, y, out_dtype, s);
   if (is8(d->format)) return launch_dequant8(*d, codes, scales, tensor_scale_dev, y, out_dtype, s);
   return launch_dequant4(*d, codes, scales, tensor_scale_dev, y, out_dtype, s);
 }
@@ -315,8 +329,27 @@ extern "C" qz_status qz_error_stats(const qz_desc* d, const void* x, const void*
   if (!aligned(x, d->in_dtype == QZ_BF16 ? 2 : 4)) return QZ_ERR_ALIGN;
   if (d->granularity == QZ_GRAN_ROW && !aligned(scales, 4)) return QZ_ERR_ALIGN;
   if (tensor_scale_dev && !aligned(tensor_scale_dev, 4)) return QZ_ERR_ALIGN;
+  if (isint4(d->format)) return launch_stats_int4(*d, x, codes, scales, stats_dev, ws, s);
   if (is8(d->format)) return launch_stats8(*d, x, codes, scales, tensor_scale_dev, stats_dev, ws, s);
   return launch_stats4(*d, x, codes, scales, tensor_scale_dev, stats_dev, ws, s);
+}
+
+extern "C" qz_status qz_dequantize_asym4(const uint32_t* w, const float* scales,
+                                         const uint32_t* shifts, int64_t rows, int64_t cols,
+                                         int64_t group, void* y, int64_t ld, int32_t out_dtype,
+                                         qz_stream_t stream) {
+  qz_status st = check_dtype(out_dtype);
+  if (st != QZ_OK) return st;
+  if (rows < 0 || cols < 0 || ld < cols || group <= 0 || cols % 8 != 0 || cols % group != 0)
+    return QZ_ERR_SHAPE;
+  if (rows > 0 && ld > 0 && rows > (INT64_MAX / 8) / ld) return QZ_ERR_SHAPE;
+  if (rows * cols == 0) return QZ_OK;
+  if (!w || !scales || !shifts || !y) return QZ_ERR_NULL;
+  if (!aligned(w, 4) || !aligned(scales, 4) || !aligned(shifts, 4) ||
+      !aligned(y, out_dtype == QZ_BF16 ? 2 : 4))
+    return QZ_ERR_ALIGN;
+  return launch_dequant_asym4(w, scales, shifts, rows, cols, group, y, ld, out_dtype,
+                              reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" qz_status qz_get_device_status(const void* ws, uint32_t* flags_host, qz_stream_t stream) {

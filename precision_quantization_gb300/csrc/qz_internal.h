@@ -49,6 +49,17 @@ qz_status launch_stats4(const qz_desc& d, const void* x, const void* codes,
                         cudaStream_t s);
 qz_status launch_empty(float* tscale_out, qz_stats* stats, cudaStream_t s);
 
+// grouped symmetric INT4 (block_size = group) and the asymmetric 4-bit group dequantize
+qz_status launch_quant_int4(const qz_desc& d, const void* x, void* codes, void* scales,
+                            float* tscale_out, qz_stats* stats, void* ws, cudaStream_t s);
+qz_status launch_stats_int4(const qz_desc& d, const void* x, const void* codes, const void* scales,
+                            qz_stats* stats, void* ws, cudaStream_t s);
+qz_status launch_dequant_int4(const qz_desc& d, const void* codes, const void* scales, void* y,
+                              int out_dtype, cudaStream_t s);
+qz_status launch_dequant_asym4(const uint32_t* w, const float* scales, const uint32_t* shifts,
+                               int64_t rows, int64_t cols, int64_t group, void* y, int64_t ld,
+                               int out_dtype, cudaStream_t s);
+
 inline qz_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? QZ_OK : QZ_ERR_CUDA;
 }

@@ -42,7 +42,7 @@ def to_host_bits(t) -> np.ndarray:
 
 
 def run_gpu(x_np, fmt, gran, scale_round=0, tensor_amax=None, stats=True, ld_pad=0,
-            out_dtypes=("bf16", "f32")):
+            out_dtypes=("bf16", "f32"), block_size=None):
     import precision_quantization_gb300 as qz
     torch = torch_mod()
     x = to_device(x_np, ld_pad)
@@ -50,7 +50,8 @@ def run_gpu(x_np, fmt, gran, scale_round=0, tensor_amax=None, stats=True, ld_pad
     ta = None
     if tensor_amax is not None:
         ta = torch.tensor([tensor_amax], dtype=torch.float32, device=x.device)
-    q, st = qz.quantize(x, fmt, gran, scale_round, ta, stats=stats, workspace=ws)
+    q, st = qz.quantize(x, fmt, gran, scale_round, ta, stats=stats, workspace=ws,
+                        block_size=block_size)
     ys = {}
     for od in out_dtypes:
         dt = torch.bfloat16 if od == "bf16" else torch.float32
@@ -69,13 +70,15 @@ def run_gpu(x_np, fmt, gran, scale_round=0, tensor_amax=None, stats=True, ld_pad
 
 
 def run_oracle(x_np, fmt, gran, scale_round=0, tensor_amax=None, stats=True,
-               out_dtypes=("bf16", "f32")):
+               out_dtypes=("bf16", "f32"), block_size=None):
     rows, cols = x_np.shape
-    codes, scales, ts, st = O.quantize(x_np, fmt, gran, scale_round, tensor_amax, stats)
+    codes, scales, ts, st = O.quantize(x_np, fmt, gran, scale_round, tensor_amax, stats,
+                                       block_size=block_size)
     y = {}
     for od in out_dtypes:
         odt = O.BF16 if od == "bf16" else O.F32
-        yy = O.dequantize(codes, scales, ts, fmt, gran, rows, cols, out_dtype=odt)
+        yy = O.dequantize(codes, scales, ts, fmt, gran, rows, cols, out_dtype=odt,
+                          block_size=block_size)
         y[od] = yy if odt == O.BF16 else yy.view(np.uint32)
     if scales is not None and scales.dtype == np.float32:
         scales = scales.view(np.uint32)

@@ -140,6 +140,33 @@ def test_quantize_delayed_argument_errors(qz):
                                         None) == qz.QZ_ERR_NULL
 
 
+def test_int4_descriptor_rules(qz):
+    for bs in (16, 32, 64, 128):
+        d = qz.make_desc("int4", qz.QZ_BF16, "block", 4, 256, block_size=bs)
+        assert qz.qz_quantize(d, None, FAKE, FAKE, None, None, None, None) == qz.QZ_ERR_NULL  # x
+    for bs in (0, 8, 48, 256):
+        d = qz.make_desc("int4", qz.QZ_BF16, "block", 4, 256)
+        d.block_size = bs
+        assert qz.qz_quantize(d, FAKE, FAKE, FAKE, None, None, None, None) == qz.QZ_ERR_UNSUPPORTED
+    d = qz.make_desc("int4", qz.QZ_BF16, "tensor", 4, 256)
+    assert qz.qz_quantize(d, FAKE, FAKE, FAKE, FAKE, None, None, FAKE) == qz.QZ_ERR_UNSUPPORTED
+    d = qz.make_desc("int4", qz.QZ_F32, "block", 4, 80, block_size=32)   # cols % 32 != 0
+    assert qz.qz_quantize(d, FAKE, FAKE, FAKE, None, None, None, None) == qz.QZ_ERR_SHAPE
+    d = qz.make_desc("int4", qz.QZ_F32, "block", 4, 64, block_size=32)
+    assert qz.qz_quantize(d, FAKE, FAKE, None, None, None, None, None) == qz.QZ_ERR_NULL  # scales
+    assert qz.qz_quantize(d, FAKE, FAKE, FAKE + 2, None, None, None, None) == qz.QZ_ERR_ALIGN
+
+
+def test_asym4_argument_errors_host(qz):
+    F = FAKE
+    assert qz.qz_dequantize_asym4(F, F, F, 2, 20, 4, F, 20, qz.QZ_F32) == qz.QZ_ERR_SHAPE
+    assert qz.qz_dequantize_asym4(F, F, F, 2, 64, 24, F, 64, qz.QZ_F32) == qz.QZ_ERR_SHAPE
+    assert qz.qz_dequantize_asym4(F, F, F, 2, 64, 16, F, 32, qz.QZ_F32) == qz.QZ_ERR_SHAPE  # ld
+    assert qz.qz_dequantize_asym4(None, F, F, 2, 64, 16, F, 64, qz.QZ_F32) == qz.QZ_ERR_NULL
+    assert qz.qz_dequantize_asym4(F, F, F, 2, 64, 16, F + 2, 64, qz.QZ_F32) == qz.QZ_ERR_ALIGN
+    assert qz.qz_dequantize_asym4(F, F, F, 2, 64, 16, F, 64, 9) == qz.QZ_ERR_ENUM
+
+
 def test_dequantize_and_stats_argument_errors(qz):
     d = qz.make_desc("mxfp4", qz.QZ_BF16, "block", 4, 64)
     assert qz.qz_dequantize(d, FAKE, FAKE, None, FAKE, 5) == qz.QZ_ERR_ENUM
