@@ -16,6 +16,7 @@
 
 #include "qz_device.cuh"
 #include "qz_internal.h"
+#include "qz_pipe.cuh"
 
 namespace qz {
 namespace {
@@ -170,6 +171,156 @@ __global__ void __launch_bounds__(kThreads) int4_quant_kernel(I4Args a) {
     }
   }
   if constexpr (STATS) stats_finish(acc, a.ws, a.stats, static_cast<uint64_t>(g.rows * g.cols));
+}
+
+// ---- staged path (dense, 16-byte aligned x): the quant4 tile pipeline ---------------
+// One 32-byte chunk: group amax, scale, quotients (fp32 pairs), integer rounding, nibble
+// packing, stores, and (STATS) the error.  |x| <= A and s = fl32(A/7) keep |fl32(x/s)|
+// within 7 (1 + 2^-22) whenever A is normal, so the rounded q already lies in [-7, 7];
+// groups with a subnormal A (or a zero scale replaced by 1) clamp first.
+template <int DT, int G, bool STATS, bool REL>
+__device__ __forceinline__ void i4_chunk(const I4Args& a, const uint32_t (&w)[8], int64_t u,
+                                         bool valid, int lane, StatAcc& acc, float& tpart,
+                                         float zero) {
+  constexpr int EPC = Elem<DT>::kPer32B;
+  constexpr int L = G / EPC;
+  constexpr int NP = EPC / 2;
+  uint64_t xp[NP];
+#pragma unroll
+  for (int p = 0; p < NP; ++p) {
+    if constexpr (DT == QZ_BF16) xp[p] = widen_bf16x2(w[p]);
+    else xp[p] = pk(__uint_as_float(w[2 * p]), __uint_as_float(w[2 * p + 1]));
+  }
+  float A = 0.0f;
+#pragma unroll
+  for (int p = 0; p < NP; ++p) {
+    float x0, x1;
+    upk(xp[p], x0, x1);
+    A = absmax3(A, x0, x1);
+  }
+#pragma unroll
+  for (int o = 1; o < L; o <<= 1) A = absmax_nan(A, __shfl_xor_sync(kFull, A, o));
+  if (valid && !is_finite_f(A)) flag_status(a.ws, QZ_FLAG_NONFINITE_INPUT);
+
+  float s = div7(A);
+  if (s == 0.0f) s = 1.0f;
+  const float r = __frcp_rn(s);
+  const bool fast = fast_div_ok(s) && __fmul_rn(A, r) <= 0x1p126f;
+  uint64_t vp[NP];
+  if (__all_sync(kFull, fast)) {
+    const uint64_t r2 = pk(r, r), ns2 = pk(-s, -s);
+#pragma unroll
+    for (int p = 0; p < NP; ++p) vp[p] = div2(xp[p], r2, ns2);
+  } else {
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+      float x0, x1;
+      upk(xp[p], x0, x1);
+      vp[p] = fast ? div2(xp[p], pk(r, r), pk(-s, -s)) : pk(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
+    }
+  }
+  if (!__all_sync(kFull, A >= 0x1p-100f || A == 0.0f)) {
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+      float v0, v1;
+      upk(vp[p], v0, v1);
+      vp[p] = pk(fminf(fmaxf(v0, -7.0f), 7.0f), fminf(fmaxf(v1, -7.0f), 7.0f));
+    }
+  }
+  // t = v + 1.5 * 2^23: RNE to an integer; its low field bits are q (two's complement)
+  const uint64_t magic2 = pk(kMagic, kMagic);
+  uint64_t tp[NP];
+#pragma unroll
+  for (int p = 0; p < NP; ++p) tp[p] = add2(vp[p], magic2);
+  uint32_t cw[EPC / 8];
+#pragma unroll
+  for (int g8 = 0; g8 < EPC / 8; ++g8) {
+    uint32_t by[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float t0, t1;
+      upk(tp[4 * g8 + i], t0, t1);
+      // bits [0,4) from t0, bits [4,8) from t1 (the other bits are discarded below)
+      by[i] = (__float_as_uint(t0) & 0x0Fu) | (__float_as_uint(t1) << 4 & ~0x0Fu);
+    }
+    cw[g8] = __byte_perm(__byte_perm(by[0], by[1], 0x0040), __byte_perm(by[2], by[3], 0x0040), 0x5410);
+  }
+  {  // predicated stores
+    uint8_t* cp = a.codes + u * (EPC / 2);
+    const uint32_t pv = valid ? 1u : 0u, ps = (valid && lane % L == 0) ? 1u : 0u;
+    if constexpr (EPC == 16) {
+      asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %3, 0;\n\t@p st.global.v2.u32 [%0], {%1, %2};\n\t}"
+                   ::"l"(cp), "r"(cw[0]), "r"(cw[1]), "r"(pv) : "memory");
+    } else {
+      asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t@p st.global.u32 [%0], %1;\n\t}"
+                   ::"l"(cp), "r"(cw[0]), "r"(pv) : "memory");
+    }
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t@p st.global.f32 [%0], %1;\n\t}"
+                 ::"l"(a.scales + u / L), "f"(s), "r"(ps) : "memory");
+  }
+  if constexpr (STATS) {
+    const uint64_t s2 = pk(s, s), z2 = pk(zero, zero);
+    Pairs<NP> e;
+#pragma unroll
+    for (int p = 0; p < NP; ++p) e.v[p] = sub2(xp[p], mul2_rounded(sub2(tp[p], magic2), s2, z2));
+    acc_pairs<NP, REL>(acc, xp, e, tpart);
+  }
+}
+
+template <int DT, int G, bool STATS>
+__global__ void __launch_bounds__(kThreads, 3) int4_pipe_kernel(I4Args a, float zero) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bars[kPipeStages];
+  __shared__ int s_abort;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int64_t n_chunks = a.g.n_chunks;
+  if (a.tscale_out && blockIdx.x == 0 && tid == 0) *a.tscale_out = 1.0f;
+  if (tid == 0) {
+    for (int i = 0; i < kPipeStages; ++i) mbar_init(smem_addr(&bars[i]), 1);
+    mbar_init_fence();
+    s_abort = 0;
+  }
+  __syncthreads();
+  const BulkPipe<kPipeStages, kPipeTileBytes> P{smem_addr(smem), smem_addr(&bars[0]),
+                                                static_cast<const char*>(a.x), n_chunks * 32,
+                                                (n_chunks + kPipeTileChunks - 1) / kPipeTileChunks,
+                                                false};
+  if (tid == 0) P.prologue();
+  StatAcc acc;
+  for (int64_t k = 0; P.has(k); ++k) {
+    const int64_t tile = P.tile_of(k);
+    if (!P.wait(k)) s_abort = 1;
+    float tpart = 0.0f;
+    const uint32_t stage = P.stage(k);
+#pragma unroll
+    for (int c = 0; c < kPipeCPT; ++c) {
+      const int j = c * kThreads + tid;
+      const int64_t u = tile * kPipeTileChunks + j;
+      const bool valid = u < n_chunks;
+      uint32_t w[8];
+      if (valid) {
+        lds32B(w, stage + 32u * j);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = 0u;
+      }
+      if (!STATS || acc.T >= 1.0f)  // warp-uniform: the relative-error search is settled
+        i4_chunk<DT, G, STATS, false>(a, w, u, valid, lane, acc, tpart, zero);
+      else
+        i4_chunk<DT, G, STATS, true>(a, w, u, valid, lane, acc, tpart, zero);
+    }
+    if constexpr (STATS) acc_add_sum(acc, tpart);
+    __syncthreads();
+    if (s_abort) {
+      if (tid == 0) {
+        flag_status(a.ws, QZ_FLAG_PIPELINE_TIMEOUT);
+        P.drain(k);
+      }
+      return;
+    }
+    if (tid == 0) P.issue(k + kPipeStages);
+  }
+  if constexpr (STATS) stats_finish(acc, a.ws, a.stats, static_cast<uint64_t>(a.g.rows * a.g.cols));
 }
 
 // x^ of one chunk from its codes and group scale
@@ -328,6 +479,15 @@ int grid_of(K kern, int64_t work_items, int per_thread, cudaStream_t s) {
 template <int DT, int G>
 qz_status quant_g(const I4Args& a, bool stats, cudaStream_t s) {
   const int64_t chunks = a.g.n_chunks;
+  if (a.g.vec && a.g.dense && reinterpret_cast<uintptr_t>(a.x) % 16 == 0 &&
+      reinterpret_cast<uintptr_t>(a.codes) % 8 == 0) {
+    auto k = stats ? &int4_pipe_kernel<DT, G, true> : &int4_pipe_kernel<DT, G, false>;
+    if (!set_dyn_smem(reinterpret_cast<const void*>(k), static_cast<int>(kPipeSmem))) return QZ_ERR_CUDA;
+    const int grid = grid_for(reinterpret_cast<const void*>(k),
+                              (chunks + kPipeTileChunks - 1) / kPipeTileChunks, s, kPipeSmem);
+    k<<<grid, kThreads, kPipeSmem, s>>>(a, 0.0f);
+    return launch_status();
+  }
   if (stats) {
     if (a.g.vec) {
       auto k = &int4_quant_kernel<DT, G, true, true>;
