@@ -203,6 +203,13 @@ constexpr int kCPT = kPipeCPT;
 constexpr int kTileChunks = kPipeTileChunks;
 constexpr int kTileBytes = kPipeTileBytes;
 constexpr int kStages = kPipeStages;
+// tiles in flight and resident CTAs per SM of the staged quantizer, per format (measured:
+// MXFP4 gains from a fourth CTA with one stage less; NVFP4, at 72 registers, would spill)
+template <int FMT>
+struct PipeShape {
+  static constexpr int kStages = FMT == QZ_MXFP4 ? 3 : kPipeStages;
+  static constexpr int kCtas = FMT == QZ_MXFP4 ? 4 : 3;
+};
 
 // Largest magnitude of 2*NP values held as fp32 pairs, as a tree of 3-input maxima (short
 // dependency chains); NAN_PROP selects the NaN-propagating maximum.
@@ -386,9 +393,10 @@ __device__ __forceinline__ void q4_chunk(const Q4Args& a, const Q4Ctx& cx, const
 }
 
 template <int FMT, int DT, bool UNIT, bool STATS, int SR>
-__global__ void __launch_bounds__(kThreads, 3) quant4_pipe_kernel(Q4Args a) {
+__global__ void __launch_bounds__(kThreads, PipeShape<FMT>::kCtas) quant4_pipe_kernel(Q4Args a) {
+  constexpr int S = PipeShape<FMT>::kStages;
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t bars[kStages];
+  __shared__ __align__(8) uint64_t bars[S];
   __shared__ float2 tab[128];  // NVFP4: (s, RN(1/s)) for every E4M3 block code
   __shared__ int s_abort;
   const int tid = threadIdx.x, lane = tid & 31;
@@ -414,12 +422,12 @@ __global__ void __launch_bounds__(kThreads, 3) quant4_pipe_kernel(Q4Args a) {
   }
   if (a.tscale_out && blockIdx.x == 0 && tid == 0) *a.tscale_out = cx.sg;
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) mbar_init(smem_addr(&bars[i]), 1);
+    for (int i = 0; i < S; ++i) mbar_init(smem_addr(&bars[i]), 1);
     mbar_init_fence();
     s_abort = 0;
   }
   __syncthreads();
-  const BulkPipe<kStages, kTileBytes> P{smem_addr(smem), smem_addr(&bars[0]),
+  const BulkPipe<S, kTileBytes> P{smem_addr(smem), smem_addr(&bars[0]),
                                         static_cast<const char*>(a.x), n_chunks * 32,
                                         (n_chunks + kTileChunks - 1) / kTileChunks, a.reverse};
   if (tid == 0) P.prologue();
@@ -457,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 3) quant4_pipe_kernel(Q4Args a) {
       }
       return;
     }
-    if (tid == 0) P.issue(k + kStages);
+    if (tid == 0) P.issue(k + S);
   }
   if (a.amax_out) amax_finish<QZ_F32>(am, a.amax_out, a.ws);
   if constexpr (STATS) stats_finish(acc, a.ws, a.stats, static_cast<uint64_t>(a.g.rows * a.g.cols));
@@ -467,11 +475,12 @@ template <int FMT, int DT, bool UNIT, bool STATS>
 qz_status run_pipe(const Q4Args& args, cudaStream_t s) {
   auto kern = args.scale_round == QZ_SCALE_NEAREST ? &quant4_pipe_kernel<FMT, DT, UNIT, STATS, QZ_SCALE_NEAREST>
                                                     : &quant4_pipe_kernel<FMT, DT, UNIT, STATS, QZ_SCALE_UP>;
-  if (!set_dyn_smem(reinterpret_cast<const void*>(kern), static_cast<int>(kPipeSmem)))
+  constexpr size_t smem = static_cast<size_t>(PipeShape<FMT>::kStages) * kTileBytes;
+  if (!set_dyn_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem)))
     return QZ_ERR_CUDA;
   const int grid = grid_for(reinterpret_cast<const void*>(kern),
-                            (args.g.n_chunks + kTileChunks - 1) / kTileChunks, s, kPipeSmem);
-  kern<<<grid, kThreads, kPipeSmem, s>>>(args);
+                            (args.g.n_chunks + kTileChunks - 1) / kTileChunks, s, smem);
+  kern<<<grid, kThreads, smem, s>>>(args);
   return launch_status();
 }
 
