@@ -241,6 +241,14 @@ QZ_API qz_status qz_dequantize_asym4(const uint32_t* w, const float* scales,
                                      int64_t group, void* y, int64_t ld, int32_t out_dtype,
                                      qz_stream_t stream);
 
+/* Self-test of the staged kernels' failure path (the post has no counterpart; an interface
+ * matter).  Every wait of the staged kernels on their own bulk copies gives up after a
+ * limit, sets QZ_FLAG_PIPELINE_TIMEOUT in the workspace status word and returns.  This call
+ * runs that same bounded wait, with limit_ns in (0, 100 ms], on a barrier that nothing
+ * completes, so the flag must come up while the context stays usable.  Nothing faults.
+ * QZ_ERR_UNSUPPORTED for a limit outside the range; needs the workspace; asynchronous. */
+QZ_API qz_status qz_selftest_pipeline_timeout(void* ws, uint64_t limit_ns, qz_stream_t stream);
+
 /* Synchronize `stream`, then copy the workspace status word (QZ_FLAG_* bits, sticky until
  * qz_workspace_init) into *flags_host. */
 QZ_API qz_status qz_get_device_status(const void* ws, uint32_t* flags_host, qz_stream_t stream);

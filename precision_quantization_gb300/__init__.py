@@ -39,7 +39,8 @@ BLOCK_SIZE = {QZ_MXFP4: 32, QZ_NVFP4: 16, QZ_INT4: 32}  # INT4: the default grou
 # Names of the exported C symbols (the whole ABI of include/qz.h).
 ABI_SYMBOLS = ("qz_status_string", "qz_workspace_size", "qz_workspace_init", "qz_amax",
                "qz_quantize", "qz_quantize_delayed", "qz_dequantize", "qz_error_stats",
-               "qz_error_stats_noalloc", "qz_dequantize_asym4", "qz_get_device_status")
+               "qz_error_stats_noalloc", "qz_dequantize_asym4", "qz_selftest_pipeline_timeout",
+               "qz_get_device_status")
 
 
 class QzDesc(C.Structure):
@@ -87,6 +88,7 @@ def lib():
             "qz_get_device_status": (i32, [vp, C.POINTER(C.c_uint32), vp]),
             "qz_dequantize_asym4": (i32, [vp, vp, vp, C.c_int64, C.c_int64, C.c_int64, vp,
                                           C.c_int64, i32, vp]),
+            "qz_selftest_pipeline_timeout": (i32, [vp, C.c_uint64, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -130,6 +132,10 @@ def qz_dequantize_asym4(w: int, scales: int, shifts: int, rows: int, cols: int, 
                         y: int, ld: int, out_dtype: int, stream: int = 0) -> int:
     return lib().qz_dequantize_asym4(w, scales, shifts, rows, cols, group, y, ld, out_dtype,
                                      stream)
+
+
+def qz_selftest_pipeline_timeout(ws: int, limit_ns: int, stream: int = 0) -> int:
+    return lib().qz_selftest_pipeline_timeout(ws, limit_ns, stream)
 
 
 def qz_dequantize(desc: QzDesc, codes: int, scales: int | None, tensor_scale_dev: int | None,
