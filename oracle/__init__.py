@@ -73,6 +73,7 @@ def lib():
             "orc_error_stats": (i32, [i32, i32, i32, i32, i64, i64, i64, vp, vp, vp, fp, sp,
                                       i32]),
             "orc_dequant_asym4": (i32, [i64, i64, i64, vp, vp, vp, vp, i32, i32]),
+            "orc_quant_dot": (i32, [i64, i64, i64, i64, vp, vp, vp, vp, vp, vp, i32]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -244,3 +245,23 @@ def dequant_asym4(w: np.ndarray, scales: np.ndarray, shifts: np.ndarray, rows: i
                                  _ptr(y), out_dtype, nthreads)
     _check(rc, "dequant_asym4")
     return y
+
+
+def quant_dot(w: np.ndarray, scales: np.ndarray, shifts: np.ndarray, y_bf16: np.ndarray,
+              group: int, nthreads: int = 0):
+    """The puzzle's z = sum_l sc (w - sh) y, in double: returns (z, sum of |terms|), both
+    float64 [n0, n1].  w uint32 [n0, mid/8]; scales float32 [n0, mid/group]; shifts uint32
+    [n0, ceil(mid/group/8)]; y bf16 bits uint16 [mid, n1]."""
+    n0, wpr = w.shape
+    mid = wpr * 8
+    n1 = y_bf16.shape[1]
+    z = np.zeros((n0, n1), dtype=np.float64)
+    za = np.zeros((n0, n1), dtype=np.float64)
+    w = np.ascontiguousarray(w, dtype=np.uint32)
+    scales = np.ascontiguousarray(scales, dtype=np.float32)
+    shifts = np.ascontiguousarray(shifts, dtype=np.uint32)
+    y_bf16 = np.ascontiguousarray(y_bf16, dtype=np.uint16)
+    rc = lib().orc_quant_dot(n0, mid, group, n1, _ptr(w), _ptr(scales), _ptr(shifts),
+                             _ptr(y_bf16), _ptr(z), _ptr(za), nthreads)
+    _check(rc, "quant_dot")
+    return z, za

@@ -745,3 +745,34 @@ int orc_dequant_asym4(int64_t rows, int64_t cols, int64_t group, const uint32_t*
   (void)nt;
   return ORC_OK;
 }
+
+int orc_quant_dot(int64_t n0, int64_t mid, int64_t group, int64_t n1, const uint32_t* w,
+                  const float* scales, const uint32_t* shifts, const uint16_t* y, double* z,
+                  double* zabs, int nthreads) {
+  if (n0 < 0 || mid < 0 || n1 < 0 || group <= 0 || mid % 8 || mid % group) return ORC_ERR_ARG;
+  if (n0 * n1 == 0) return ORC_OK;
+  if (!w || !scales || !shifts || !y || !z) return ORC_ERR_ARG;
+  const int64_t ng = mid / group, sw = (ng + 7) / 8;
+  const int nt = nthreads_of(nthreads);
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(nt)
+#endif
+  for (int64_t j = 0; j < n0; ++j) {
+    for (int64_t k = 0; k < n1; ++k) {
+      double s = 0.0, sa = 0.0;
+      for (int64_t l = 0; l < mid; ++l) {
+        const int64_t g = l / group;
+        const int q = (int)word_nibble(w + j * (mid / 8), l);
+        const int sh = (int)word_nibble(shifts + j * sw, g);
+        const float deq = get_f32(scales, j * ng + g) * (float)(q - sh); /* one binary32 rounding */
+        const double p = (double)deq * orc_decode_bf16(y[l * n1 + k]);
+        s += p;
+        sa += fabs(p);
+      }
+      z[j * n1 + k] = s;
+      if (zabs) zabs[j * n1 + k] = sa;
+    }
+  }
+  (void)nt;
+  return ORC_OK;
+}

@@ -107,6 +107,19 @@ int orc_dequant_asym4(int64_t rows, int64_t cols, int64_t group, const uint32_t*
                       const float* scales, const uint32_t* shifts, void* y, int out_dtype,
                       int nthreads);
 
+/* The puzzle's quantized matrix product z[j][k] = sum_l sc (w[j][l] - sh) * y[l][k]:
+ *   w, scales, shifts as orc_dequant_asym4 ([n0, mid] weights in groups of `group`);
+ *   y [mid, n1] bf16 bit patterns (row-major, leading dimension n1);
+ *   z [n0, n1] double: the dequantized weight taken as the binary32 value of
+ *     orc_dequant_asym4's fp32 output, each product and the sum in double -- every product
+ *     of a binary32 and a bf16 value is exact in double and the sum of mid of them is
+ *     accurate to mid * 2^-53 of the sum of magnitudes;
+ *   zabs [n0, n1] double (may be NULL): sum_l |deq * y|, the scale of the rounding error
+ *     of any evaluation order. */
+int orc_quant_dot(int64_t n0, int64_t mid, int64_t group, int64_t n1, const uint32_t* w,
+                  const float* scales, const uint32_t* shifts, const uint16_t* y, double* z,
+                  double* zabs, int nthreads);
+
 #ifdef __cplusplus
 }
 #endif

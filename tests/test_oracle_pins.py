@@ -618,3 +618,42 @@ def test_asym4_identity_order_and_groups(orc):
     assert np.array_equal(y, (sc[:, gi] * (codes - shv[:, gi])).astype(np.float32))
     yb = orc.dequant_asym4(w, sc, sh, rows, cols, group, out_dtype=orc.BF16)
     assert np.array_equal(yb, (y.view(np.uint32) >> 16).astype(np.uint16))  # exact in bf16
+
+
+def test_quant_dot_worked_example(orc):
+    g = golden("puzzle12_asym_dequant.json")
+    ex, dx = g["example"], g["dot_example"]
+    w = np.array([ex["w_words"]], dtype=np.uint32)
+    y = np.full((16, 1), 0x3F80, dtype=np.uint16)          # bf16 1.0
+    z, za = orc.quant_dot(w, np.array([[ex["scale"]]], np.float32),
+                          np.array([[ex["shift"]]], np.uint32), y, ex["group"])
+    assert z[0, 0] == dx["z"]
+    assert za[0, 0] == sum(abs(v) for v in ex["y"])
+
+
+def test_quant_dot_integer_and_dyadic_exact(orc):
+    """With small integers (sc = 1, sh = 0) the product is an integer matrix product; with
+    power-of-two scales and shifts every term and sum is a small dyadic rational, exact in
+    float64, so numpy's matmul of the dequantized matrix gives the exact answer."""
+    rng = np.random.default_rng(45)
+    n0, mid, n1, group = 6, 128, 5, 32
+    codes = rng.integers(0, 16, (n0, mid))
+    w = np.zeros((n0, mid // 8), dtype=np.uint32)
+    for j in range(8):
+        w |= codes[:, j::8].astype(np.uint32) << np.uint32(4 * j)
+    yi = rng.integers(-8, 9, (mid, n1))
+    y = (np.float32(1.0) * yi).astype(np.float32).view(np.uint32) >> 16   # exact in bf16
+    y = y.astype(np.uint16)
+    ng = mid // group
+    z, za = orc.quant_dot(w, np.ones((n0, ng), np.float32), np.zeros((n0, 1), np.uint32), y, group)
+    assert np.array_equal(z, (codes @ yi).astype(np.float64))
+    assert np.array_equal(za, (np.abs(codes) @ np.abs(yi)).astype(np.float64))
+    sc = (2.0 ** rng.integers(-3, 4, (n0, ng))).astype(np.float32)
+    shv = rng.integers(0, 16, (n0, ng))
+    sh = np.zeros((n0, 1), dtype=np.uint32)
+    for j in range(ng):
+        sh[:, 0] |= shv[:, j].astype(np.uint32) << np.uint32(4 * j)
+    gi = np.arange(mid) // group
+    deq = sc[:, gi].astype(np.float64) * (codes - shv[:, gi])
+    z, _ = orc.quant_dot(w, sc, sh, y, group)
+    assert np.array_equal(z, deq @ yi.astype(np.float64))
