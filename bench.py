@@ -160,10 +160,11 @@ class ClockSampler:
 MATRIX = [
     (1, None, [("int8", "tensor"), ("e4m3", "tensor"), ("mxfp4", "block"), ("nvfp4", "block")]),
     (2, None, [("int8", "row"), ("e4m3", "row"), ("mxfp4", "block"), ("nvfp4", "block"),
-               ("int4", "block", 128), ("asym4", "group", 128)]),
+               ("int4", "block", 128), ("asym4", "group", 128), ("qdot", "group", 128, 1),
+               ("qdot", "group", 128, 8)]),
     (3, None, [("e4m3", "row"), ("e5m2", "row"), ("nvfp4", "block"), ("nvfp4", "block", "delayed")]),
     (4, None, [("mxfp4", "block"), ("nvfp4", "block"), ("nvfp4", "block", "delayed"),
-               ("int4", "block", 32)]),
+               ("int4", "block", 32), ("qdot", "group", 128, 8)]),
     (5, 4096, [(f, g) for f in ("int8", "e4m3", "e5m2") for g in ("unit", "tensor")] +
               [(f, g) for f in ("mxfp4", "nvfp4") for g in ("unit", "block")] +
               [("e4m3", "tensor", "delayed"), ("nvfp4", "block", "delayed")]),
@@ -218,6 +219,9 @@ def measure_matrix(dev, peaks, flush, x4=None, reps=10, which=(1, 2, 3, 4, 5)) -
             fname, gname = run[0], run[1]
             if fname == "asym4":
                 out.append(measure_asym4(name, r, c, run[2], timed, peaks, dev))
+                continue
+            if fname == "qdot":
+                out.append(measure_qdot(name, r, c, run[2], run[3], timed, peaks, dev))
                 continue
             delayed = len(run) > 2 and run[2] == "delayed"
             bsz = run[2] if len(run) > 2 and isinstance(run[2], int) else None
@@ -288,6 +292,37 @@ def measure_asym4(name, rows, cols, group, timed, peaks, dev) -> dict:
             "quantize_launches": 0,
             "dequantize_us": round(dms * 1e3, 1), "dequantize_gbs": round(db / dms / 1e6, 1),
             "dequantize_frac": round(db / dms / 1e6 / peaks["hbm_gbs"], 3)}
+
+
+def measure_qdot(name, n0, mid, group, n1, timed, peaks, dev) -> dict:
+    """The quantized matrix product z = sum sc (w - sh) y with a weight of the workload's
+    shape ([n0, mid], seeded random codes, shifts and scales made on the device) and n1
+    bf16 activation columns.  Reported in the dequantize columns: GB/s of weights, scales,
+    shifts, activations and outputs moved."""
+    import torch
+    import precision_quantization_gb300 as qz
+    gen = torch.Generator(device=dev).manual_seed(11)
+    w = torch.randint(-2 ** 31, 2 ** 31 - 1, (n0, mid // 8), dtype=torch.int32, device=dev,
+                      generator=gen)
+    ng = mid // group
+    sc = torch.randn((n0, ng), dtype=torch.float32, device=dev, generator=gen) * 0.02
+    sh = torch.randint(-2 ** 31, 2 ** 31 - 1, (n0, (ng + 7) // 8), dtype=torch.int32,
+                       device=dev, generator=gen)
+    y = torch.randn((mid, n1), dtype=torch.float32, device=dev, generator=gen).to(torch.bfloat16)
+    z = torch.empty((n0, n1), dtype=torch.float32, device=dev)
+    sp = torch.cuda.current_stream(dev).cuda_stream
+
+    def run():
+        rc = qz.qz_quant_dot(w.data_ptr(), sc.data_ptr(), sh.data_ptr(), n0, mid, group,
+                             y.data_ptr(), n1, n1, z.data_ptr(), n1, sp)
+        assert rc == 0, rc
+    ms = timed(run)
+    nb = (w.numel() + sc.numel() + sh.numel()) * 4 + y.numel() * 2 + z.numel() * 4
+    return {"workload": name, "format": "qdot", "granularity": f"group {group} n1 {n1}",
+            "quantize_us": None, "quantize_gbs": None, "quantize_frac": None,
+            "quantize_launches": 0,
+            "dequantize_us": round(ms * 1e3, 1), "dequantize_gbs": round(nb / ms / 1e6, 1),
+            "dequantize_frac": round(nb / ms / 1e6 / peaks["hbm_gbs"], 3)}
 
 
 def dist_setup():

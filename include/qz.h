@@ -241,6 +241,21 @@ QZ_API qz_status qz_dequantize_asym4(const uint32_t* w, const float* scales,
                                      int64_t group, void* y, int64_t ld, int32_t out_dtype,
                                      qz_stream_t stream);
 
+/* The quantized matrix product of "Puzzles 12 Quantized Matrix Mult" (Triton post):
+ *   z[j][k] = sum_l sc[j][l / group] * (w[j][l] - sh[j][l / group]) * y[l][k]
+ *   w, scales, shifts  device, the weights [n0, mid] exactly as qz_dequantize_asym4 (rows =
+ *                      n0, cols = mid): each weight is fl32(sc * (w - sh)), as that call writes
+ *   y                  device, bf16 activations [mid, ld_y], ld_y >= n1, 2-byte aligned
+ *   z                  device, fp32 [n0, ld_z], ld_z >= n1, 4-byte aligned
+ * Each product weight * y is accumulated in fp32 by FMA, in an unspecified order: every
+ * z[j][k] is within (mid + 6) * 2^-24 * sum_l |weight * y| of the exact sum.
+ * n1 in [1, 8] (few activation columns: the product streams the packed weights once and
+ * is bound by HBM); larger n1 gives QZ_ERR_UNSUPPORTED.  mid % 8 == 0, group > 0,
+ * mid % group == 0 (QZ_ERR_SHAPE).  Asynchronous on `stream`; needs no workspace. */
+QZ_API qz_status qz_quant_dot(const uint32_t* w, const float* scales, const uint32_t* shifts,
+                              int64_t n0, int64_t mid, int64_t group, const void* y, int64_t ld_y,
+                              int64_t n1, float* z, int64_t ld_z, qz_stream_t stream);
+
 /* Self-test of the staged kernels' failure path (the post has no counterpart; an interface
  * matter).  Every wait of the staged kernels on their own bulk copies gives up after a
  * limit, sets QZ_FLAG_PIPELINE_TIMEOUT in the workspace status word and returns.  This call

@@ -39,8 +39,8 @@ BLOCK_SIZE = {QZ_MXFP4: 32, QZ_NVFP4: 16, QZ_INT4: 32}  # INT4: the default grou
 # Names of the exported C symbols (the whole ABI of include/qz.h).
 ABI_SYMBOLS = ("qz_status_string", "qz_workspace_size", "qz_workspace_init", "qz_amax",
                "qz_quantize", "qz_quantize_delayed", "qz_dequantize", "qz_error_stats",
-               "qz_error_stats_noalloc", "qz_dequantize_asym4", "qz_selftest_pipeline_timeout",
-               "qz_get_device_status")
+               "qz_error_stats_noalloc", "qz_dequantize_asym4", "qz_quant_dot",
+               "qz_selftest_pipeline_timeout", "qz_get_device_status")
 
 
 class QzDesc(C.Structure):
@@ -89,6 +89,8 @@ def lib():
             "qz_dequantize_asym4": (i32, [vp, vp, vp, C.c_int64, C.c_int64, C.c_int64, vp,
                                           C.c_int64, i32, vp]),
             "qz_selftest_pipeline_timeout": (i32, [vp, C.c_uint64, vp]),
+            "qz_quant_dot": (i32, [vp, vp, vp, C.c_int64, C.c_int64, C.c_int64, vp, C.c_int64,
+                                   C.c_int64, vp, C.c_int64, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -132,6 +134,27 @@ def qz_dequantize_asym4(w: int, scales: int, shifts: int, rows: int, cols: int, 
                         y: int, ld: int, out_dtype: int, stream: int = 0) -> int:
     return lib().qz_dequantize_asym4(w, scales, shifts, rows, cols, group, y, ld, out_dtype,
                                      stream)
+
+
+def qz_quant_dot(w: int, scales: int, shifts: int, n0: int, mid: int, group: int, y: int,
+                 ld_y: int, n1: int, z: int, ld_z: int, stream: int = 0) -> int:
+    return lib().qz_quant_dot(w, scales, shifts, n0, mid, group, y, ld_y, n1, z, ld_z, stream)
+
+
+def quant_dot(w, scales, shifts, group: int, y, out=None, stream=None):
+    """z = sum_l sc (w - sh) y (see qz_quant_dot): w int32/uint32 CUDA tensor [n0, mid/8],
+    scales fp32 [n0, mid/group], shifts int32/uint32 [n0, ceil(mid/group/8)], y bf16
+    [mid, n1] (n1 <= 8).  Returns fp32 [n0, n1]."""
+    torch = _torch()
+    n0, wpr = w.shape
+    mid, n1 = y.shape
+    if mid != wpr * 8:
+        raise ValueError("y must have mid = 8 * w.shape[1] rows")
+    z = out if out is not None else torch.empty((n0, n1), dtype=torch.float32, device=w.device)
+    _check(qz_quant_dot(w.data_ptr(), scales.data_ptr(), shifts.data_ptr(), n0, mid, group,
+                        y.data_ptr(), y.stride(0), n1, z.data_ptr(), z.stride(0),
+                        _stream(stream)), "qz_quant_dot")
+    return z
 
 
 def qz_selftest_pipeline_timeout(ws: int, limit_ns: int, stream: int = 0) -> int:

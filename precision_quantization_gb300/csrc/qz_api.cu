@@ -352,6 +352,30 @@ extern "C" qz_status qz_dequantize_asym4(const uint32_t* w, const float* scales,
                               reinterpret_cast<cudaStream_t>(stream));
 }
 
+extern "C" qz_status qz_quant_dot(const uint32_t* w, const float* scales, const uint32_t* shifts,
+                                  int64_t n0, int64_t mid, int64_t group, const void* y,
+                                  int64_t ld_y, int64_t n1, float* z, int64_t ld_z,
+                                  qz_stream_t stream) {
+  if (n0 < 0 || mid < 0 || n1 < 0 || group <= 0 || mid % 8 != 0 || mid % group != 0 || ld_y < n1 ||
+      ld_z < n1)
+    return QZ_ERR_SHAPE;
+  if (n1 > 8) return QZ_ERR_UNSUPPORTED;
+  if ((mid > 0 && ld_y > 0 && mid > (INT64_MAX / 8) / ld_y) || (n0 > 0 && ld_z > 0 && n0 > (INT64_MAX / 8) / ld_z))
+    return QZ_ERR_SHAPE;
+  if (n0 * n1 == 0) return QZ_OK;
+  if (!w || !scales || !shifts || !y || !z) return QZ_ERR_NULL;
+  if (!aligned(w, 4) || !aligned(scales, 4) || !aligned(shifts, 4) || !aligned(y, 2) || !aligned(z, 4))
+    return QZ_ERR_ALIGN;
+  if (mid == 0) {  // empty sums
+    return cudaMemset2DAsync(z, static_cast<size_t>(ld_z) * 4, 0, static_cast<size_t>(n1) * 4,
+                             static_cast<size_t>(n0), reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? QZ_OK
+               : QZ_ERR_CUDA;
+  }
+  return launch_quant_dot(w, scales, shifts, n0, mid, group, y, ld_y, n1, z, ld_z,
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
 extern "C" qz_status qz_get_device_status(const void* ws, uint32_t* flags_host, qz_stream_t stream) {
   if (!ws || !flags_host) return QZ_ERR_NULL;
   if (!aligned(ws, 16)) return QZ_ERR_ALIGN;

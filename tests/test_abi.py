@@ -167,6 +167,17 @@ def test_asym4_argument_errors_host(qz):
     assert qz.qz_dequantize_asym4(F, F, F, 2, 64, 16, F, 64, 9) == qz.QZ_ERR_ENUM
 
 
+def test_quant_dot_argument_errors_host(qz):
+    F = FAKE
+    qd = qz.qz_quant_dot
+    assert qd(F, F, F, 4, 64, 16, F, 9, 9, F, 9) == qz.QZ_ERR_UNSUPPORTED       # n1 > 8
+    assert qd(F, F, F, 4, 60, 4, F, 8, 8, F, 8) == qz.QZ_ERR_SHAPE              # mid % 8
+    assert qd(F, F, F, 4, 64, 24, F, 8, 8, F, 8) == qz.QZ_ERR_SHAPE             # mid % group
+    assert qd(F, F, F, 4, 64, 16, F, 4, 8, F, 8) == qz.QZ_ERR_SHAPE             # ld_y < n1
+    assert qd(None, F, F, 4, 64, 16, F, 8, 8, F, 8) == qz.QZ_ERR_NULL
+    assert qd(F, F, F, 4, 64, 16, F + 1, 8, 8, F, 8) == qz.QZ_ERR_ALIGN
+
+
 def test_dequantize_and_stats_argument_errors(qz):
     d = qz.make_desc("mxfp4", qz.QZ_BF16, "block", 4, 64)
     assert qz.qz_dequantize(d, FAKE, FAKE, None, FAKE, 5) == qz.QZ_ERR_ENUM

@@ -1,0 +1,65 @@
+"""GPU parity of the quantized matrix product (qz_quant_dot) against the oracle's exact
+double sum: every output within (mid + 6) 2^-24 of the sum of the terms' magnitudes, the
+bound fp32 accumulation in any order guarantees (include/qz.h)."""
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as W
+from gpu_util import torch_mod
+
+pytestmark = pytest.mark.gpu
+
+
+def pack_words(vals):
+    rows, n = vals.shape
+    out = np.zeros((rows, (n + 7) // 8), dtype=np.uint32)
+    for i in range(n):
+        out[:, i // 8] |= vals[:, i].astype(np.uint32) << np.uint32(4 * (i % 8))
+    return out
+
+
+def make(n0, mid, group, n1, seed):
+    rng = np.random.default_rng(seed)
+    ng = mid // group
+    w = pack_words(rng.integers(0, 16, (n0, mid)))
+    sc = (rng.standard_normal((n0, ng)) * 0.02).astype(np.float32)
+    sh = pack_words(rng.integers(0, 16, (n0, ng)))
+    y = W.bf16_bits(W.normal(mid, max(n1, 1), 1.0, seed=seed + 1, dtype="f32"))[:, :n1]
+    return w, sc, sh, np.ascontiguousarray(y)
+
+
+@pytest.mark.parametrize("ypad,zpad", [(0, 0), (8, 3), (5, 0)])
+@pytest.mark.parametrize("n0,mid,group,n1", [(1, 8, 8, 1), (7, 64, 16, 3), (33, 1024, 128, 8),
+                                             (128, 4096, 32, 5), (5, 96, 12, 2), (64, 256, 256, 1),
+                                             (300, 2048, 64, 4), (9, 520, 40, 7)])
+def test_quant_dot_parity(n0, mid, group, n1, ypad, zpad):
+    import precision_quantization_gb300 as qz
+    torch = torch_mod()
+    w, sc, sh, y = make(n0, mid, group, n1, seed=930 + n0 + mid)
+    zr, za = O.quant_dot(w, sc, sh, y, group)
+    yb = torch.zeros((mid, n1 + ypad), dtype=torch.int16, device="cuda")
+    yb[:, :n1] = torch.from_numpy(y.view(np.int16)).cuda()
+    yd = yb.view(torch.bfloat16)[:, :n1]
+    zb = torch.full((n0, n1 + zpad), 7.0, dtype=torch.float32, device="cuda")
+    z = qz.quant_dot(torch.from_numpy(w.view(np.int32)).cuda(), torch.from_numpy(sc).cuda(),
+                     torch.from_numpy(sh.view(np.int32)).cuda(), group, yd, out=zb[:, :n1])
+    torch.cuda.synchronize()
+    got = z.cpu().numpy().astype(np.float64)
+    tol = (mid + 6) * 2.0 ** -24 * za + 1e-35
+    assert np.all(np.abs(got - zr) <= tol), float(np.max(np.abs(got - zr) - tol))
+    assert np.all(zb[:, n1:].cpu().numpy() == 7.0)  # nothing written past n1
+
+
+def test_quant_dot_weight_like_shape():
+    """A 4096 x 4096 weight (the weight-like workload's shape) in groups of 128, 8 columns."""
+    import precision_quantization_gb300 as qz
+    torch = torch_mod()
+    n0 = mid = 4096
+    w, sc, sh, y = make(n0, mid, 128, 8, seed=950)
+    zr, za = O.quant_dot(w, sc, sh, y, 128)
+    z = qz.quant_dot(torch.from_numpy(w.view(np.int32)).cuda(), torch.from_numpy(sc).cuda(),
+                     torch.from_numpy(sh.view(np.int32)).cuda(), 128,
+                     torch.from_numpy(y.view(np.int16)).cuda().view(torch.bfloat16))
+    got = z.cpu().numpy().astype(np.float64)
+    assert np.all(np.abs(got - zr) <= (mid + 6) * 2.0 ** -24 * za + 1e-35)
