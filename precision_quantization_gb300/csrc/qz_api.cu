@@ -43,6 +43,20 @@ int g_launch_n = 0;
 int g_sms[kCacheDevices];
 }  // namespace
 
+int sm_count() {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  {
+    std::lock_guard<std::mutex> lock(g_launch_mu);
+    if (dev >= 0 && dev < kCacheDevices && g_sms[dev] > 0) return g_sms[dev];
+  }
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (sms < 1) sms = 1;
+  std::lock_guard<std::mutex> lock(g_launch_mu);
+  if (dev >= 0 && dev < kCacheDevices) g_sms[dev] = sms;
+  return sms;
+}
+
 int grid_for(const void* kernel, int64_t work_ctas, cudaStream_t, size_t dyn_smem) {
   int dev = 0, sms = 1, occ = 1;
   cudaGetDevice(&dev);

@@ -24,6 +24,9 @@ Geom make_geom(const qz_desc& d, const void* hp, int elem_bytes, int align_bytes
 // the partial-result slots of the workspace.
 int grid_for(const void* kernel, int64_t work_ctas, cudaStream_t stream, size_t dyn_smem = 0);
 
+// SM count of the current device (cached).
+int sm_count();
+
 // Opt `kernel` in to `bytes` of dynamic shared memory on the current device (once).
 bool set_dyn_smem(const void* kernel, int bytes);
 
