@@ -247,8 +247,9 @@ QZ_API qz_status qz_dequantize_asym4(const uint32_t* w, const float* scales,
  *                      n0, cols = mid): each weight is fl32(sc * (w - sh)), as that call writes
  *   y                  device, bf16 activations [mid, ld_y], ld_y >= n1, 2-byte aligned
  *   z                  device, fp32 [n0, ld_z], ld_z >= n1, 4-byte aligned
- * Each product weight * y is accumulated in fp32 by FMA, in an unspecified order: every
- * z[j][k] is within (mid + 6) * 2^-24 * sum_l |weight * y| of the exact sum.
+ * The sum runs in fp32 in an unspecified order -- with group % 16 == 0 on the tensor cores
+ * as sum over groups of sc * sum (w - sh) y, whose integer factors are exact in bf16 --
+ * and every z[j][k] is within (2 mid + 8) * 2^-24 * sum_l |weight * y| of the exact sum.
  * n1 in [1, 8] (few activation columns: the product streams the packed weights once and
  * is bound by HBM); larger n1 gives QZ_ERR_UNSUPPORTED.  mid % 8 == 0, group > 0,
  * mid % group == 0 (QZ_ERR_SHAPE).  Asynchronous on `stream`; needs no workspace. */
