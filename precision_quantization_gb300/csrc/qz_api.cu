@@ -381,10 +381,7 @@ extern "C" qz_status qz_quant_dot(const uint32_t* w, const float* scales, const 
   if (!aligned(w, 4) || !aligned(scales, 4) || !aligned(shifts, 4) || !aligned(y, 2) || !aligned(z, 4))
     return QZ_ERR_ALIGN;
   if (mid == 0) {  // empty sums
-    return cudaMemset2DAsync(z, static_cast<size_t>(ld_z) * 4, 0, static_cast<size_t>(n1) * 4,
-                             static_cast<size_t>(n0), reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
-               ? QZ_OK
-               : QZ_ERR_CUDA;
+    return launch_zero_z(z, ld_z, n0, n1, reinterpret_cast<cudaStream_t>(stream));
   }
   return launch_quant_dot(w, scales, shifts, n0, mid, group, y, ld_y, n1, z, ld_z,
                           reinterpret_cast<cudaStream_t>(stream));

@@ -62,6 +62,8 @@ qz_status launch_dequant_int4(const qz_desc& d, const void* codes, const void* s
 qz_status launch_dequant_asym4(const uint32_t* w, const float* scales, const uint32_t* shifts,
                                int64_t rows, int64_t cols, int64_t group, void* y, int64_t ld,
                                int out_dtype, cudaStream_t s);
+// z[j][0 .. n1) = 0 for j < n0 (rows ld_z floats apart)
+qz_status launch_zero_z(float* z, int64_t ld_z, int64_t n0, int64_t n1, cudaStream_t s);
 qz_status launch_quant_dot(const uint32_t* w, const float* scales, const uint32_t* shifts,
                            int64_t n0, int64_t mid, int64_t group, const void* y, int64_t ld_y,
                            int64_t n1, float* z, int64_t ld_z, cudaStream_t s);

@@ -31,6 +31,14 @@ struct QdArgs {
   int64_t wps;        // code words per slice, a multiple of 32
 };
 
+// z[j][0 .. n1) = 0 for the split sums to add into (a 2-D memset of 4 * n1-byte rows)
+__global__ void __launch_bounds__(kThreads) zero_z_kernel(float* z, int64_t ld_z, int64_t n0, int n1) {
+  const int64_t n = n0 * n1;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * kThreads)
+    z[(i / n1) * ld_z + i % n1] = 0.0f;
+}
+
 __device__ __forceinline__ float bf16_value(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
 
 // x + 1.5 * 2^23 read back as a float minus 1.5 * 2^23: the small integer d, exactly
@@ -145,18 +153,42 @@ __global__ void __launch_bounds__(kThreads) quant_dot_kernel(QdArgs a, bool yvec
   }
 }
 
-// ---- tensor-core form (group % 16 == 0, mid % 32 == 0) ----------------------------------
+// ---- tensor-core form (group % 16 == 0, mid % 64 == 0) ----------------------------------
 // sum_l sc (w - sh) y = sum_groups sc_g * sum_{l in g} (w - sh) y: w - sh is an integer in
 // [-15, 15], exact in bf16, and so is every product with a bf16 y in fp32, so the inner
 // sums run on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate) and the
 // group scale is applied by one FMA per output and group.  The rounding of this order
 // stays within the bound qz_quant_dot states for any order of the fp32 terms.
 //
-// A warp owns 16 weight rows and one slice of l; the 8 warps of a CTA share the slice,
-// whose activations are staged in shared memory as yT[n][l] (n < 8, zero past n1, rows
-// padded by 8 elements so the fragment reads are conflict-free).
-constexpr int kQdSliceMax = 2048;          // l per slice (staged activations: 8 x 2056 bf16)
+// Work item: 128 weight rows (16 per warp) x one slice of l.  Per item the CTA stages in
+// shared memory the slice's activations as rows of 8 bf16 (ys[l][n], zero past n1) and the
+// rows' scales and shift words for the groups the slice touches; each warp streams its
+// rows' code words through a ring of kQdBatches batches of 256 values of l: 128 contiguous
+// bytes of each of its 16 rows per batch (whole DRAM bursts; runs of 32 bytes per row
+// left the memory at a third of its bandwidth), four 16-byte cp.async per lane, two
+// batches in flight while the third is consumed in 64-wide steps.  Activations (n1 == 8,
+// aligned rows), scales, shifts and code words all move by cp.async.
+//
+// The k order inside a 16-wide part is permuted, the same way for both operands (a sum
+// does not depend on the naming of its index): mma slots (2t, 2t+1, 2t+8, 2t+9) of lane
+// t hold l = (t, t+4, 8+t, 12+t).  Then the weight pair a lane needs from one code word is
+// its nibbles t and t+4, i.e. (word >> 4t) & 0x000F000F, which OR 0x43004300 turns into the
+// bf16 pair (128 + w_t, 128 + w_t+4); one bf16x2 FMA subtracts 128 + sh exactly.  The B
+// fragments come from ys by ldmatrix.trans, whose per-lane row addresses apply the same
+// permutation (row r of an 8 x 8 tile <-> slot r <-> l = r / 2 + 4 (r % 2)).
+constexpr int kQdSlice = 1024;                 // max l per slice
+constexpr int kQdBatch = 4;                    // 64-wide steps per batch of code words
+constexpr int kQdBatches = 3;                  // batches in the ring of a warp
+constexpr int kQdStages = kQdBatch * kQdBatches;
 constexpr int kQdRowsPerCta = 16 * kWarps;
+constexpr int kQdGroups = 17;                  // groups a slice may touch (slice <= 16 groups)
+
+struct QdSmem {
+  uint4 ys[kQdSlice];  // activation row l: y[l][0 .. 8) as bf16
+  uint32_t wbuf[kWarps][kQdStages][16][8];
+  float sc[kQdRowsPerCta][kQdGroups];
+  uint32_t shw[kQdRowsPerCta][3];  // the shift words covering those groups
+};
 
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -166,107 +198,296 @@ __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], const uint32_t (&a
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// bf16 pair (lo, hi) of the nibbles i and i + 1 of `word` minus the shift, exact integers:
-// base = 0x4B400000 - sh, so base + nibble is the encoding of 1.5 * 2^23 + (w - sh)
-__device__ __forceinline__ uint32_t int_pair_bf16(uint32_t word, int i, uint32_t base) {
-  const uint32_t lo = base + ((word >> (4 * i)) & 0xFu);
-  const uint32_t hi = base + ((word >> (4 * i + 4)) & 0xFu);
-  const uint64_t v = sub2(pk(__uint_as_float(lo), __uint_as_float(hi)), pk(kMagic, kMagic));
-  float vl, vh;
-  upk(v, vl, vh);
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(vh), "f"(vl));
+// the bf16 pair (w_t - sh, w_t+4 - sh) of a code word already shifted right by 4t;
+// nsh = the bf16 pair (-(128 + sh), -(128 + sh))
+__device__ __forceinline__ uint32_t weight_pair(uint32_t shifted, uint32_t nsh) {
+  uint32_t x, r;
+  asm("lop3.b32 %0, %1, 0x000F000F, 0x43004300, 0xEA;" : "=r"(x) : "r"(shifted));  // (a & b) | c
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(0x3F803F80u), "r"(nsh));  // x * 1 + nsh
   return r;
 }
 
-__global__ void __launch_bounds__(kThreads) quant_dot_mma_kernel(QdArgs a, int n1) {
-  __shared__ uint16_t yT[8][kQdSliceMax + 8];
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr) : "memory");
+}
+
+// Quotient by an invariant divisor d by one multiply (Granlund and Montgomery, "Division
+// by invariant integers using multiplication", 1994): with l = ceil(log2 d) and
+// m = floor(2^32 (2^l - d) / d) + 1, n / d = (umulhi(m, n) + n) >> l for 0 <= n < 2^31.
+struct FastDiv {
+  uint32_t m = 1, l = 0;
+  FastDiv() = default;
+  explicit FastDiv(uint32_t d) {
+    while ((1ull << l) < d) ++l;
+    m = static_cast<uint32_t>(((1ull << 32) * ((1ull << l) - d)) / d + 1);
+  }
+  __device__ __forceinline__ int operator()(int n) const {
+    return static_cast<int>((__umulhi(m, static_cast<uint32_t>(n)) + static_cast<uint32_t>(n)) >> l);
+  }
+};
+
+struct QmArgs {
+  const uint32_t* w;
+  const float* scales;
+  const uint32_t* shifts;
+  const uint16_t* y;  // bf16 bits [mid, ld_y]
+  float* z;
+  int64_t n0, ld_y, ld_z, wpr, ng, sw;  // wpr: code words per row; ng / sw: groups / shift words per row
+  int mid, group, lps, ksplit, nitems;  // lps: l per slice (a multiple of 64); items = row blocks x slices
+  FastDiv by_ksplit, by_group;
+};
+
+// G64: group % 64 == 0, so groups change only between 64-wide steps
+template <bool G64>
+__global__ void __launch_bounds__(kThreads, 3) quant_dot_mma_kernel(QmArgs a, int n1, bool yvec) {
+  extern __shared__ __align__(16) unsigned char qd_smem_raw[];
+  QdSmem& sm = *reinterpret_cast<QdSmem*>(qd_smem_raw);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
-  const int64_t wpr = a.mid / 8, ng = a.mid / a.group, sw = (ng + 7) / 8;
-  const int64_t nrb = (a.n0 + kQdRowsPerCta - 1) / kQdRowsPerCta;
-  for (int64_t item = blockIdx.x; item < nrb * a.ksplit; item += gridDim.x) {
-    const int64_t r0 = (item / a.ksplit) * kQdRowsPerCta + warp * 16;
-    const int64_t l_begin = (item % a.ksplit) * a.wps * 8;
-    const int64_t l_len = min(a.wps * 8, a.mid - l_begin);  // a multiple of 32
-    __syncthreads();  // the previous item's staged activations are no longer read
-    for (int l = threadIdx.x; l < l_len; l += kThreads) {
-      const uint16_t* yr = a.y + (l_begin + l) * a.ld_y;
+  constexpr uint32_t kStageBytes = 16 * 8 * 4;
+  // ldmatrix row address of this lane: tile m = lane / 8 (part m / 2, slots 8 (m % 2) ..),
+  // row r = lane % 8 <-> l = 16 (m / 2) + 8 (m % 2) + r / 2 + 4 (r % 2)
+  const int mt = lane >> 3, mr = lane & 7;
+  const uint32_t yl = static_cast<uint32_t>(__cvta_generic_to_shared(
+      &sm.ys[16 * (mt >> 1) + 8 * (mt & 1) + (mr >> 1) + 4 * (mr & 1)]));
+  const uint32_t wl = static_cast<uint32_t>(__cvta_generic_to_shared(&sm.wbuf[warp][0][g][0]));
+  // the copies of a lane: 16 bytes of row 4 j + lane / 8, chunk lane % 8 of a batch (step
+  // chunk / 2, half chunk % 2)
+  const int cchunk = lane & 7, crow = warp * 16 + (lane >> 3);  // CTA-local row of copy 0
+  const uint32_t cdst0 = static_cast<uint32_t>(
+      __cvta_generic_to_shared(&sm.wbuf[warp][cchunk >> 1][lane >> 3][4 * (cchunk & 1)]));
+  const int ra = warp * 16 + g, rb = ra + 8;  // CTA-local rows of this lane's outputs
+
+  for (int item = blockIdx.x; item < a.nitems; item += gridDim.x) {
+    const int kb = a.by_ksplit(item);
+    const int64_t rc = static_cast<int64_t>(kb) * kQdRowsPerCta;  // first row of the CTA
+    const int rlast = static_cast<int>(min(static_cast<int64_t>(kQdRowsPerCta - 1), a.n0 - 1 - rc));
+    const int l_begin = (item - kb * a.ksplit) * a.lps;
+    const int l_len = min(a.lps, a.mid - l_begin);  // a multiple of 64
+    const int g_first = a.by_group(l_begin);
+    const int ngs = a.by_group(l_begin + l_len - 1) - g_first + 1;  // <= kQdGroups
+    const int nsteps = l_len / 64, nbatches = (nsteps + kQdBatch - 1) / kQdBatch;
+    const bool live = warp * 16 <= rlast;
+    __syncthreads();  // the previous item's staged data is no longer read
+
+    // scales and shift words of the CTA's rows for the groups g_first .. g_first + ngs - 1,
+    // by 4-byte asynchronous copies (rows past the end are left as they are: their
+    // outputs are not written).  Entry idx -> (row idx / n, idx % n); the quotient by a
+    // float reciprocal is exact here: (idx + 1/2) / n lies at least 1 / (2 n) from an
+    // integer, and idx < 2^12.
+    const int gfo = g_first & 7;                // nibble of g_first in its shift word
+    const int nsw = (gfo + ngs + 7) / 8;        // shift words per row, <= 3
+    {
+      const float* sbase = a.scales + rc * a.ng + g_first;
+      const float rcp = 1.0f / static_cast<float>(ngs);
+      for (int idx = threadIdx.x; idx < kQdRowsPerCta * ngs; idx += kThreads) {
+        const int rr = static_cast<int>((static_cast<float>(idx) + 0.5f) * rcp), gi = idx - rr * ngs;
+        if (rr <= rlast)
+          cp_async4(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.sc[rr][gi])), sbase + rr * a.ng + gi);
+      }
+      const uint32_t* hbase = a.shifts + rc * a.sw + (g_first >> 3);
+      const float rcpw = 1.0f / static_cast<float>(nsw);
+      for (int idx = threadIdx.x; idx < kQdRowsPerCta * nsw; idx += kThreads) {
+        const int rr = static_cast<int>((static_cast<float>(idx) + 0.5f) * rcpw), k = idx - rr * nsw;
+        if (rr <= rlast)
+          cp_async4(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.shw[rr][k])), hbase + rr * a.sw + k);
+      }
+    }
+    // activations of the slice: rows of 16 bytes
+    const uint16_t* ybase = a.y + static_cast<int64_t>(l_begin) * a.ld_y;
+    if (yvec) {  // n1 == 8, rows 16-byte aligned: copied as they are
+      for (int l = threadIdx.x; l < l_len; l += kThreads)
+        cp_async16(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.ys[l])), ybase + l * a.ld_y);
+    } else {  // zero past n1
+      for (int l = threadIdx.x; l < l_len; l += kThreads) {
+        const uint16_t* yr = ybase + l * a.ld_y;
+        uint32_t v[4];
 #pragma unroll
-      for (int n = 0; n < 8; ++n) yT[n][l] = n < n1 ? yr[n] : static_cast<uint16_t>(0);
+        for (int n = 0; n < 4; ++n) {
+          const uint32_t lo = 2 * n < n1 ? __ldg(yr + 2 * n) : 0u;
+          const uint32_t hi = 2 * n + 1 < n1 ? __ldg(yr + 2 * n + 1) : 0u;
+          v[n] = lo | (hi << 16);
+        }
+        sm.ys[l] = make_uint4(v[0], v[1], v[2], v[3]);
+      }
+    }
+    cp_async_commit();  // scales, shifts and activations: one group, older than the code words'
+
+    // this warp's code words, a batch at a time (rows past the end are not copied)
+    const uint32_t* csrc = a.w + (rc + crow) * a.wpr + l_begin / 8 + 4 * cchunk;
+    const int64_t cstride = 4 * a.wpr;  // 4 rows
+    int ahead = 0;     // batches issued so far
+    int bt_issue = 0;  // ring slot of the next one
+    const auto issue = [&]() {
+      if (ahead < nbatches && kQdBatch * ahead + (cchunk >> 1) < nsteps) {
+        const uint32_t dst = cdst0 + bt_issue * (kQdBatch * kStageBytes);
+        const uint32_t* src = csrc + 32 * ahead;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (crow + 4 * j <= rlast) cp_async16(dst + j * 4 * 32, src + j * cstride);
+      }
+      cp_async_commit();  // empty groups keep the count uniform
+      ++ahead;
+      bt_issue = bt_issue == kQdBatches - 1 ? 0 : bt_issue + 1;
+    };
+    if (live) {
+#pragma unroll
+      for (int i = 0; i < kQdBatches - 1; ++i) issue();
+      cp_async_wait<kQdBatches - 1>();  // the scale group (older than the code words)
+    } else {
+      cp_async_wait<0>();
     }
     __syncthreads();
-    const int64_t ra = min(r0 + g, a.n0 - 1), rb = min(r0 + g + 8, a.n0 - 1);  // rows of this lane
+    if (!live) continue;  // a warp past the last row: nothing below synchronises the CTA
+
     float z[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // rows g / g+8, columns 2t, 2t+1
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    int64_t cur = -1;  // group of acc
-    float sca = 0.0f, scb = 0.0f;
-    uint32_t sha = 0u, shb = 0u;  // 0x4B400000 - shift of rows g / g+8
-    if (r0 < a.n0) {
-      for (int64_t l = 0; l < l_len; l += 32) {
-        const int64_t lg = l_begin + l;      // global l of this 32-wide step
-        const uint4 wa = __ldg(reinterpret_cast<const uint4*>(a.w + ra * wpr + lg / 8));
-        const uint4 wb = __ldg(reinterpret_cast<const uint4*>(a.w + rb * wpr + lg / 8));
-        const uint32_t wra[4] = {wa.x, wa.y, wa.z, wa.w}, wrb[4] = {wb.x, wb.y, wb.z, wb.w};
-#pragma unroll
-        for (int s = 0; s < 2; ++s) {       // two k16 steps
-          const int64_t k0 = lg + 16 * s;
-          const int64_t grp = k0 / a.group;
-          if (grp != cur) {                  // close the previous group: z += sc * acc
-            z[0] = __fmaf_rn(sca, acc[0], z[0]);
-            z[1] = __fmaf_rn(sca, acc[1], z[1]);
-            z[2] = __fmaf_rn(scb, acc[2], z[2]);
-            z[3] = __fmaf_rn(scb, acc[3], z[3]);
-            acc[0] = acc[1] = acc[2] = acc[3] = 0.0f;
-            cur = grp;
-            sca = __ldg(a.scales + ra * ng + grp);
-            scb = __ldg(a.scales + rb * ng + grp);
-            sha = 0x4B400000u - ((__ldg(a.shifts + ra * sw + grp / 8) >> (4 * (grp % 8))) & 0xFu);
-            shb = 0x4B400000u - ((__ldg(a.shifts + rb * sw + grp / 8) >> (4 * (grp % 8))) & 0xFu);
-          }
-          uint32_t af[4];
-          af[0] = int_pair_bf16(wra[2 * s], 2 * t, sha);      // row g,   k 2t, 2t+1
-          af[1] = int_pair_bf16(wrb[2 * s], 2 * t, shb);      // row g+8, k 2t, 2t+1
-          af[2] = int_pair_bf16(wra[2 * s + 1], 2 * t, sha);  // row g,   k 2t+8, 2t+9
-          af[3] = int_pair_bf16(wrb[2 * s + 1], 2 * t, shb);  // row g+8, k 2t+8, 2t+9
-          const int64_t kl = l + 16 * s + 2 * t;               // slice-local k of b0
-          const uint32_t b0 = *reinterpret_cast<const uint32_t*>(&yT[g][kl]);
-          const uint32_t b1 = *reinterpret_cast<const uint32_t*>(&yT[g][kl + 8]);
-          mma_bf16_16816(acc, af, b0, b1);
-        }
-      }
+    int gi = 0;  // staged group of acc
+    // its l still to come, in 64- or 16-wide units
+    int left = ((g_first + 1) * a.group - l_begin) / (G64 ? 64 : 16);
+    const int per = a.group / (G64 ? 64 : 16);
+    // -(128 + sh) as a bf16 pair, for staged group gi of CTA-local row r
+    const auto nshift = [&](int r, int gi) {
+      const int p = gfo + gi;
+      return 0xC300C300u + 0x00010001u * ((sm.shw[r][p >> 3] >> (4 * (p & 7))) & 0xFu);
+    };
+    float sca = sm.sc[ra][0], scb = sm.sc[rb][0];
+    uint32_t nsa = nshift(ra, 0), nsb = nshift(rb, 0);
+    const auto next_group = [&]() {  // z += sc * acc for the group just closed; load the next
       z[0] = __fmaf_rn(sca, acc[0], z[0]);
       z[1] = __fmaf_rn(sca, acc[1], z[1]);
       z[2] = __fmaf_rn(scb, acc[2], z[2]);
       z[3] = __fmaf_rn(scb, acc[3], z[3]);
+      acc[0] = acc[1] = acc[2] = acc[3] = 0.0f;
+      ++gi;
+      sca = sm.sc[ra][gi];
+      scb = sm.sc[rb][gi];
+      nsa = nshift(ra, gi);
+      nsb = nshift(rb, gi);
+    };
+    int slot = 0;  // ring slot of batch bt
+#pragma unroll 1
+    for (int bt = 0; bt < nbatches; ++bt) {
+      cp_async_wait<kQdBatches - 2>();  // this lane's copies of batch bt have landed
+      __syncwarp();                     // ... and every lane's; batch bt - 1 is read
+      issue();
+      const uint32_t wsl = wl + slot * (kQdBatch * kStageBytes);
+      const uint32_t ysl = yl + bt * (kQdBatch * 64 * 16);
+      slot = slot == kQdBatches - 1 ? 0 : slot + 1;
+      const int nq = min(kQdBatch, nsteps - kQdBatch * bt);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int64_t row = r0 + g + (i >= 2 ? 8 : 0);
-        const int col = 2 * t + (i & 1);
-        if (row < a.n0 && col < n1) {
-          float* zp = a.z + row * a.ld_z + col;
-          if (a.ksplit > 1) atomicAdd(zp, z[i]);
-          else *zp = z[i];
+      for (int q = 0; q < kQdBatch; ++q) {  // the batch's 64-wide steps
+        if (q >= nq) break;
+        const uint32_t wst = wsl + q * kStageBytes;
+        const uint4 wa0 = lds128(wst), wa1 = lds128(wst + 16);                    // row g
+        const uint4 wb0 = lds128(wst + 8 * 32), wb1 = lds128(wst + 8 * 32 + 16);  // row g + 8
+        uint32_t yb[8];  // B registers (b0, b1) of parts 0 .. 3
+        ldsm_x4_trans(*reinterpret_cast<uint32_t(*)[4]>(&yb[0]), ysl + q * 64 * 16);            // parts 0, 1
+        ldsm_x4_trans(*reinterpret_cast<uint32_t(*)[4]>(&yb[4]), ysl + q * 64 * 16 + 32 * 16);  // parts 2, 3
+        if (G64) {
+          if (left == 0) {
+            next_group();
+            left = per;
+          }
+          --left;
         }
+        const uint32_t wa[8] = {wa0.x, wa0.y, wa0.z, wa0.w, wa1.x, wa1.y, wa1.z, wa1.w};
+        const uint32_t wb[8] = {wb0.x, wb0.y, wb0.z, wb0.w, wb1.x, wb1.y, wb1.z, wb1.w};
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {  // four k16 parts
+          if (!G64) {
+            if (left == 0) {
+              next_group();
+              left = per;
+            }
+            --left;
+          }
+          uint32_t af[4];
+          af[0] = weight_pair(wa[2 * s] >> (4 * t), nsa);      // row g,   slots 2t, 2t+1
+          af[1] = weight_pair(wb[2 * s] >> (4 * t), nsb);      // row g+8, slots 2t, 2t+1
+          af[2] = weight_pair(wa[2 * s + 1] >> (4 * t), nsa);  // row g,   slots 2t+8, 2t+9
+          af[3] = weight_pair(wb[2 * s + 1] >> (4 * t), nsb);  // row g+8, slots 2t+8, 2t+9
+          mma_bf16_16816(acc, af, yb[2 * s], yb[2 * s + 1]);
+        }
+      }
+    }
+    cp_async_wait<0>();
+    __syncwarp();
+    z[0] = __fmaf_rn(sca, acc[0], z[0]);
+    z[1] = __fmaf_rn(sca, acc[1], z[1]);
+    z[2] = __fmaf_rn(scb, acc[2], z[2]);
+    z[3] = __fmaf_rn(scb, acc[3], z[3]);
+    float* zr = a.z + (rc + ra) * a.ld_z + 2 * t;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int row = ra + (q >= 2 ? 8 : 0), col = 2 * t + (q & 1);
+      if (row <= rlast && col < n1) {
+        float* zp = zr + (q >= 2 ? 8 * a.ld_z : 0) + (q & 1);
+        if (a.ksplit > 1) atomicAdd(zp, z[q]);
+        else *zp = z[q];
       }
     }
   }
 }
 
-qz_status run_mma(QdArgs a, int n1, cudaStream_t s) {
-  const int64_t wpr = a.mid / 8, nrb = (a.n0 + kQdRowsPerCta - 1) / kQdRowsPerCta;
-  const int64_t want = static_cast<int64_t>(sm_count()) * 2;  // CTAs
-  int64_t ks = std::max<int64_t>((want + nrb - 1) / nrb, (a.mid + kQdSliceMax - 1) / kQdSliceMax);
-  ks = std::max<int64_t>(1, std::min<int64_t>(ks, wpr / 4));
-  a.wps = ((wpr + ks - 1) / ks + 3) / 4 * 4;  // words per slice: l a multiple of 32
-  a.ksplit = (wpr + a.wps - 1) / a.wps;
-  if (a.ksplit > 1 &&
-      cudaMemset2DAsync(a.z, static_cast<size_t>(a.ld_z) * 4, 0, static_cast<size_t>(n1) * 4,
-                        static_cast<size_t>(a.n0), s) != cudaSuccess)
-    return QZ_ERR_CUDA;
-  const int grid = grid_for(reinterpret_cast<const void*>(&quant_dot_mma_kernel), nrb * a.ksplit, s);
-  quant_dot_mma_kernel<<<grid, kThreads, 0, s>>>(a, static_cast<int>(n1));
-  return launch_status();
+// false when the sizes leave the 32-bit index range the kernel assumes
+bool run_mma(QdArgs in, int n1, bool yvec, cudaStream_t s, qz_status* st) {
+  const int64_t wpr = in.mid / 8, nrb = (in.n0 + kQdRowsPerCta - 1) / kQdRowsPerCta;
+  // a slice spans at most 16 groups (so it touches at most kQdGroups) and kQdSlice values
+  const int64_t lmax = std::min<int64_t>(kQdSlice, 16 * in.group);  // a multiple of 256
+  const int64_t want = static_cast<int64_t>(sm_count()) * 2;        // CTAs
+  int64_t ks = std::max<int64_t>((want + nrb - 1) / nrb, (in.mid + lmax - 1) / lmax);
+  ks = std::max<int64_t>(1, std::min<int64_t>(ks, wpr / 8));
+  const int64_t wps = ((wpr + ks - 1) / ks + 7) / 8 * 8;  // words per slice: l a multiple of 64
+  const int64_t ksplit = (wpr + wps - 1) / wps;
+  if (in.mid + in.group >= (int64_t{1} << 31) || nrb * ksplit >= (int64_t{1} << 31)) return false;
+  QmArgs a;
+  a.w = in.w;
+  a.scales = in.scales;
+  a.shifts = in.shifts;
+  a.y = in.y;
+  a.z = in.z;
+  a.n0 = in.n0;
+  a.ld_y = in.ld_y;
+  a.ld_z = in.ld_z;
+  a.wpr = wpr;
+  a.ng = in.mid / in.group;
+  a.sw = (a.ng + 7) / 8;
+  a.mid = static_cast<int>(in.mid);
+  a.group = static_cast<int>(in.group);
+  a.lps = static_cast<int>(wps * 8);
+  a.ksplit = static_cast<int>(ksplit);
+  a.nitems = static_cast<int>(nrb * ksplit);
+  a.by_ksplit = FastDiv(static_cast<uint32_t>(ksplit));
+  a.by_group = FastDiv(static_cast<uint32_t>(in.group));
+  const bool g64 = in.group % 64 == 0;
+  const void* k = g64 ? reinterpret_cast<const void*>(&quant_dot_mma_kernel<true>)
+                      : reinterpret_cast<const void*>(&quant_dot_mma_kernel<false>);
+  const int smem = static_cast<int>(sizeof(QdSmem));
+  *st = QZ_ERR_CUDA;
+  if (!set_dyn_smem(k, smem)) return true;
+  if (ksplit > 1 && launch_zero_z(in.z, in.ld_z, in.n0, n1, s) != QZ_OK) return true;
+  const int grid = grid_for(k, a.nitems, s, smem);
+  if (g64) quant_dot_mma_kernel<true><<<grid, kThreads, smem, s>>>(a, n1, yvec);
+  else quant_dot_mma_kernel<false><<<grid, kThreads, smem, s>>>(a, n1, yvec);
+  *st = launch_status();
+  return true;
 }
 
 template <int N1>
@@ -280,10 +501,7 @@ qz_status run(QdArgs a, bool yvec, cudaStream_t s) {
   ks = std::max<int64_t>(1, std::min<int64_t>(ks, wpr / 32));
   a.wps = ((wpr + ks - 1) / ks + 31) / 32 * 32;
   a.ksplit = (wpr + a.wps - 1) / a.wps;
-  if (a.ksplit > 1 &&
-      cudaMemset2DAsync(a.z, static_cast<size_t>(a.ld_z) * 4, 0, static_cast<size_t>(N1) * 4,
-                        static_cast<size_t>(a.n0), s) != cudaSuccess)
-    return QZ_ERR_CUDA;
+  if (a.ksplit > 1 && launch_zero_z(a.z, a.ld_z, a.n0, N1, s) != QZ_OK) return QZ_ERR_CUDA;
   const int grid = grid_for(reinterpret_cast<const void*>(k),
                             (nblocks * a.ksplit + kWarps - 1) / kWarps, s);
   k<<<grid, kThreads, 0, s>>>(a, yvec);
@@ -292,13 +510,23 @@ qz_status run(QdArgs a, bool yvec, cudaStream_t s) {
 
 }  // namespace
 
+qz_status launch_zero_z(float* z, int64_t ld_z, int64_t n0, int64_t n1, cudaStream_t s) {
+  const int64_t n = n0 * n1;
+  if (n == 0) return QZ_OK;
+  const int64_t ctas = std::min<int64_t>((n + kThreads - 1) / kThreads, static_cast<int64_t>(sm_count()) * 8);
+  zero_z_kernel<<<static_cast<int>(ctas), kThreads, 0, s>>>(z, ld_z, n0, static_cast<int>(n1));
+  return launch_status();
+}
+
 qz_status launch_quant_dot(const uint32_t* w, const float* scales, const uint32_t* shifts,
                            int64_t n0, int64_t mid, int64_t group, const void* y, int64_t ld_y,
                            int64_t n1, float* z, int64_t ld_z, cudaStream_t s) {
   const QdArgs a{w, scales, shifts, static_cast<const uint16_t*>(y), z, n0, mid, group, ld_y, ld_z, 1, 0};
-  if (group % 16 == 0 && mid % 32 == 0 && reinterpret_cast<uintptr_t>(w) % 16 == 0)
-    return run_mma(a, static_cast<int>(n1), s);
   const bool yvec = reinterpret_cast<uintptr_t>(y) % 16 == 0 && ld_y % 8 == 0;
+  qz_status st = QZ_OK;
+  if (group % 16 == 0 && mid % 64 == 0 && reinterpret_cast<uintptr_t>(w) % 16 == 0 &&
+      run_mma(a, static_cast<int>(n1), yvec && n1 == 8, s, &st))
+    return st;
   switch (n1) {
     case 1: return run<1>(a, yvec, s);
     case 2: return run<2>(a, yvec, s);

@@ -32,7 +32,9 @@ def make(n0, mid, group, n1, seed):
 @pytest.mark.parametrize("ypad,zpad", [(0, 0), (8, 3), (5, 0)])
 @pytest.mark.parametrize("n0,mid,group,n1", [(1, 8, 8, 1), (7, 64, 16, 3), (33, 1024, 128, 8),
                                              (128, 4096, 32, 5), (5, 96, 12, 2), (64, 256, 256, 1),
-                                             (300, 2048, 64, 4), (9, 520, 40, 7)])
+                                             (300, 2048, 64, 4), (9, 520, 40, 7),
+                                             (17, 96, 32, 8), (40, 192, 48, 6), (129, 8192, 128, 8),
+                                             (260, 640, 16, 2)])
 def test_quant_dot_parity(n0, mid, group, n1, ypad, zpad):
     import precision_quantization_gb300 as qz
     torch = torch_mod()
