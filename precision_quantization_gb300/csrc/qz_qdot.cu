@@ -163,11 +163,10 @@ __global__ void __launch_bounds__(kThreads) quant_dot_kernel(QdArgs a, bool yvec
 // Work item: 128 weight rows (16 per warp) x one slice of l.  Per item the CTA stages in
 // shared memory the slice's activations as rows of 8 bf16 (ys[l][n], zero past n1) and the
 // rows' scales and shift words for the groups the slice touches; each warp streams its
-// rows' code words through a ring of kQdBatches batches of 256 values of l: 128 contiguous
-// bytes of each of its 16 rows per batch (whole DRAM bursts; runs of 32 bytes per row
-// left the memory at a third of its bandwidth), four 16-byte cp.async per lane, two
-// batches in flight while the third is consumed in 64-wide steps.  Activations (n1 == 8,
-// aligned rows), scales, shifts and code words all move by cp.async.
+// rows' code words through a ring of kQdBatches batches of kQdBatch 64-wide steps (32
+// kQdBatch contiguous bytes of each of its 16 rows per batch, 16-byte cp.async), the
+// later batches in flight while the first is consumed.  Activations (n1 == 8, aligned
+// rows), scales, shifts and code words all move by cp.async.
 //
 // The k order inside a 16-wide part is permuted, the same way for both operands (a sum
 // does not depend on the naming of its index): mma slots (2t, 2t+1, 2t+8, 2t+9) of lane
@@ -177,7 +176,7 @@ __global__ void __launch_bounds__(kThreads) quant_dot_kernel(QdArgs a, bool yvec
 // fragments come from ys by ldmatrix.trans, whose per-lane row addresses apply the same
 // permutation (row r of an 8 x 8 tile <-> slot r <-> l = r / 2 + 4 (r % 2)).
 constexpr int kQdSlice = 1024;                 // max l per slice
-constexpr int kQdBatch = 4;                    // 64-wide steps per batch of code words
+constexpr int kQdBatch = 4;                    // 64-wide steps per batch of code words (2 or 4)
 constexpr int kQdBatches = 3;                  // batches in the ring of a warp
 constexpr int kQdStages = kQdBatch * kQdBatches;
 constexpr int kQdRowsPerCta = 16 * kWarps;
@@ -267,11 +266,14 @@ __global__ void __launch_bounds__(kThreads, 3) quant_dot_mma_kernel(QmArgs a, in
   const uint32_t yl = static_cast<uint32_t>(__cvta_generic_to_shared(
       &sm.ys[16 * (mt >> 1) + 8 * (mt & 1) + (mr >> 1) + 4 * (mr & 1)]));
   const uint32_t wl = static_cast<uint32_t>(__cvta_generic_to_shared(&sm.wbuf[warp][0][g][0]));
-  // the copies of a lane: 16 bytes of row 4 j + lane / 8, chunk lane % 8 of a batch (step
-  // chunk / 2, half chunk % 2)
-  const int cchunk = lane & 7, crow = warp * 16 + (lane >> 3);  // CTA-local row of copy 0
+  // the copies of a lane: 16 bytes of row kRowsPerCopy j + lane / kChunks, chunk
+  // lane % kChunks of a batch (step chunk / 2, half chunk % 2)
+  constexpr int kChunks = 2 * kQdBatch;           // 16-byte chunks of a row in a batch
+  constexpr int kRowsPerCopy = 32 / kChunks;      // rows one copy instruction covers
+  constexpr int kCopies = 16 / kRowsPerCopy;      // copies per lane and batch
+  const int cchunk = lane % kChunks, crow = warp * 16 + lane / kChunks;  // CTA-local row of copy 0
   const uint32_t cdst0 = static_cast<uint32_t>(
-      __cvta_generic_to_shared(&sm.wbuf[warp][cchunk >> 1][lane >> 3][4 * (cchunk & 1)]));
+      __cvta_generic_to_shared(&sm.wbuf[warp][cchunk >> 1][lane / kChunks][4 * (cchunk & 1)]));
   const int ra = warp * 16 + g, rb = ra + 8;  // CTA-local rows of this lane's outputs
 
   for (int item = blockIdx.x; item < a.nitems; item += gridDim.x) {
@@ -331,16 +333,16 @@ __global__ void __launch_bounds__(kThreads, 3) quant_dot_mma_kernel(QmArgs a, in
 
     // this warp's code words, a batch at a time (rows past the end are not copied)
     const uint32_t* csrc = a.w + (rc + crow) * a.wpr + l_begin / 8 + 4 * cchunk;
-    const int64_t cstride = 4 * a.wpr;  // 4 rows
+    const int64_t cstride = kRowsPerCopy * a.wpr;
     int ahead = 0;     // batches issued so far
     int bt_issue = 0;  // ring slot of the next one
     const auto issue = [&]() {
       if (ahead < nbatches && kQdBatch * ahead + (cchunk >> 1) < nsteps) {
         const uint32_t dst = cdst0 + bt_issue * (kQdBatch * kStageBytes);
-        const uint32_t* src = csrc + 32 * ahead;
+        const uint32_t* src = csrc + 8 * kQdBatch * ahead;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (crow + 4 * j <= rlast) cp_async16(dst + j * 4 * 32, src + j * cstride);
+        for (int j = 0; j < kCopies; ++j)
+          if (crow + kRowsPerCopy * j <= rlast) cp_async16(dst + j * kRowsPerCopy * 32, src + j * cstride);
       }
       cp_async_commit();  // empty groups keep the count uniform
       ++ahead;
