@@ -436,7 +436,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-chunk-rows", type=int, default=4096,
+                    help="rows per host-to-device copy of the end-to-end round trip")
     ap.add_argument("--no-matrix", action="store_true",
                     help="skip the per-format matrix over the five workloads")
     ap.add_argument("--matrix-only", action="store_true",
@@ -559,35 +561,39 @@ def main():
     # ---- end to end through the public API: pinned host input in, quantized tensors out
     e2e = None
     if not args.no_e2e:
+        from precision_quantization_gb300.streamed import HostRoundTrip
         xh = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16).pin_memory()
-        host_out = {f: [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs[f]] +
-                    [torch.empty((qz.STATS_BYTES,), dtype=torch.uint8).pin_memory()]
-                    for f in outs}
-        xd = torch.empty_like(x)
-        h2d = xh.numel() * 2
-        d2h = sum(t.numel() * t.element_size() for f in outs for t in host_out[f])
-
-        def e2e_step():
-            xd.copy_(xh, non_blocking=True)
-            launches(xd.data_ptr())
-            for f in outs:
-                for hsrc, hdst in zip(list(outs[f]) + [sts[f]], host_out[f]):
-                    hdst.copy_(hsrc, non_blocking=True)
-            torch.cuda.synchronize(dev)
-
-        for _ in range(2):
-            e2e_step()
+        # the same five operations as the kernel step, on row chunks as they arrive
+        plan = HostRoundTrip(rows, COLS, [(qz.QZ_MXFP4, qz.QZ_GRAN_BLOCK),
+                                          (qz.QZ_NVFP4, qz.QZ_GRAN_BLOCK)],
+                             chunk_rows=args.e2e_chunk_rows, device=dev)
+        h2d = plan.bytes_in()
+        d2h = plan.bytes_out()
+        for _ in range(max(3, args.warmup)):
+            plan.run(xh)
         e_ms = []
         for _ in range(args.e2e_steps):
             flush.zero_()
             torch.cuda.synchronize(dev)
             t1 = time.perf_counter()
-            e2e_step()
+            plan.run(xh)
             e_ms.append((time.perf_counter() - t1) * 1e3)
-        em = max_over_ranks(statistics.mean(e_ms), world, dev)
+        if plan.ws.status() != 0:
+            raise RuntimeError("e2e: device status flags raised")
+        for j, f in enumerate((qz.QZ_MXFP4, qz.QZ_NVFP4)):  # same statistics as the kernel step
+            a, b = plan.read_stats(j), stats_host[f]
+            if a.n != b.n or a.max_abs_err != b.max_abs_err or a.max_rel_err != b.max_rel_err \
+                    or abs(a.sum_sq_err - b.sum_sq_err) > 1e-5 * abs(b.sum_sq_err):
+                raise RuntimeError(f"e2e statistics differ from the kernel step's: {a} {b}")
+        # median: a host clock around each round trip sees the odd scheduling hiccup of the
+        # host thread (tens of ms), which would dominate a mean over a few steps
+        em = max_over_ranks(statistics.median(e_ms), world, dev)
         e2e = {"value": round(job_gbs(step_bytes, world, em), 2), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": round(em, 3)}
+               "ms_per_step": round(em, 3), "ms_mean": round(statistics.mean(e_ms), 3),
+               "steps": len(e_ms), "timing": "host clock per round trip, median",
+               "chunk_rows": args.e2e_chunk_rows,
+               "api": "streamed.HostRoundTrip.run (pinned host in/out, copies overlapped)"}
 
     matrix = None
     if not args.no_matrix and rank == 0:

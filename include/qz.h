@@ -226,6 +226,18 @@ QZ_API qz_status qz_error_stats_noalloc(const qz_desc* desc, const void* x, cons
                                         const void* scales, const float* tensor_scale_dev,
                                         qz_stats* stats_dev, qz_stream_t stream);
 
+/* Statistics of one tensor from the statistics of its parts: `parts` holds `count` records
+ * (device, 8-byte aligned) written by qz_quantize / qz_error_stats over disjoint parts of
+ * the tensor (row ranges, say, quantized as they arrive).  *out (device) gets the sum of
+ * their sum_sq_err and n, mse = sum_sq_err / n (0 when n = 0), and the maximum of their
+ * max_abs_err and max_rel_err -- the statistics the definitions above give for the whole
+ * tensor (blocks never straddle a part, so the codes are the same), the sum of squares
+ * within the same 1e-5 relative bound.  The sums run in fp64 in a fixed order, so equal
+ * inputs give equal results.  `out` may be one of the parts.  count = 0 writes an empty
+ * record; count < 0 is QZ_ERR_SHAPE.  One small kernel on `stream`; no workspace. */
+QZ_API qz_status qz_stats_merge(const qz_stats* parts, int64_t count, qz_stats* out,
+                                qz_stream_t stream);
+
 /* Asymmetric 4-bit group dequantization ("Puzzles 12 Quantized Matrix Mult", Triton post):
  *   y[r][c] = fl32(sc[r][c / group] * (w[r][c] - sh[r][c / group])), w - sh exact.
  *   w       device, [rows, cols / 8] 32-bit words: 8 unsigned 4-bit codes each, element c

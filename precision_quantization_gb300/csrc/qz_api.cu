@@ -348,6 +348,14 @@ extern "C" qz_status qz_error_stats(const qz_desc* d, const void* x, const void*
   return launch_stats4(*d, x, codes, scales, tensor_scale_dev, stats_dev, ws, s);
 }
 
+extern "C" qz_status qz_stats_merge(const qz_stats* parts, int64_t count, qz_stats* out,
+                                    qz_stream_t stream) {
+  if (!out || (count > 0 && !parts)) return QZ_ERR_NULL;
+  if (count < 0) return QZ_ERR_SHAPE;
+  if (!aligned(out, 8) || (count > 0 && !aligned(parts, 8))) return QZ_ERR_ALIGN;
+  return launch_stats_merge(parts, count, out, reinterpret_cast<cudaStream_t>(stream));
+}
+
 extern "C" qz_status qz_dequantize_asym4(const uint32_t* w, const float* scales,
                                          const uint32_t* shifts, int64_t rows, int64_t cols,
                                          int64_t group, void* y, int64_t ld, int32_t out_dtype,

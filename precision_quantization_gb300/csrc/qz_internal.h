@@ -50,6 +50,8 @@ qz_status launch_stats8(const qz_desc& d, const void* x, const void* codes,
 qz_status launch_stats4(const qz_desc& d, const void* x, const void* codes,
                         const void* scales, const float* tscale, qz_stats* stats, void* ws,
                         cudaStream_t s);
+// fold `count` statistics records of disjoint parts of one tensor into *out
+qz_status launch_stats_merge(const qz_stats* parts, int64_t count, qz_stats* out, cudaStream_t s);
 qz_status launch_empty(float* tscale_out, qz_stats* stats, cudaStream_t s);
 
 // grouped symmetric INT4 (block_size = group) and the asymmetric 4-bit group dequantize

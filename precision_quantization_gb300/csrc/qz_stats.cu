@@ -174,7 +174,61 @@ qz_status launch(const qz_desc& d, const void* x, const void* codes, const void*
   }
 }
 
+// One CTA folds `count` statistics records of disjoint parts of a tensor: sums of squares
+// and element counts add (fp64, fixed order: thread t takes records t, t + 256, ..., then
+// the warp and CTA folds in lane and warp order, so a given count always sums alike), the
+// largest errors take their maximum.  Every record is read before thread 0 writes `out`,
+// so `out` may be one of the parts.
+__global__ void __launch_bounds__(kThreads) stats_merge_kernel(const qz_stats* parts, int64_t count,
+                                                               qz_stats* out) {
+  __shared__ double s_sum[kWarps];
+  __shared__ unsigned long long s_n[kWarps];
+  __shared__ float s_abs[kWarps], s_rel[kWarps];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  double t = 0.0;
+  unsigned long long n = 0;
+  float ma = 0.0f, mr = 0.0f;
+  for (int64_t i = threadIdx.x; i < count; i += kThreads) {
+    t += parts[i].sum_sq_err;
+    n += parts[i].n;
+    ma = fmaxf(ma, parts[i].max_abs_err);
+    mr = fmaxf(mr, parts[i].max_rel_err);
+  }
+  t = warp_sum(t);
+  ma = warp_max(ma);
+  mr = warp_max(mr);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) n += __shfl_xor_sync(kFull, n, o);
+  if (lane == 0) {
+    s_sum[warp] = t;
+    s_n[warp] = n;
+    s_abs[warp] = ma;
+    s_rel[warp] = mr;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double tot = 0.0;
+    unsigned long long nt = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      tot += s_sum[w];
+      nt += s_n[w];
+      ma = fmaxf(ma, s_abs[w]);
+      mr = fmaxf(mr, s_rel[w]);
+    }
+    out->sum_sq_err = tot;
+    out->mse = nt ? tot / static_cast<double>(nt) : 0.0;
+    out->max_abs_err = ma;
+    out->max_rel_err = mr;
+    out->n = nt;
+  }
+}
+
 }  // namespace
+
+qz_status launch_stats_merge(const qz_stats* parts, int64_t count, qz_stats* out, cudaStream_t s) {
+  stats_merge_kernel<<<1, kThreads, 0, s>>>(parts, count, out);
+  return launch_status();
+}
 
 qz_status launch_stats8(const qz_desc& d, const void* x, const void* codes, const void* scales,
                         const float* tscale, qz_stats* stats, void* ws, cudaStream_t s) {
