@@ -61,7 +61,7 @@ amax_kernel(const void* __restrict__ x, Geom g, float* __restrict__ out, void* w
   amax_finish<DT>(m, out, ws);
 }
 
-// Dense tensors: x streamed through shared memory by 1-D bulk copies (16 KiB tiles, four
+// Dense tensors: x streamed through shared memory by 1-D bulk copies (32 KiB tiles, two
 // in flight per CTA), so the read runs at the copy engine's pace whatever the occupancy.
 constexpr int kAmaxStages = kPipeStages;
 constexpr int kAmaxCPT = kPipeCPT;

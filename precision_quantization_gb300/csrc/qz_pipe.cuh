@@ -351,11 +351,14 @@ __device__ __forceinline__ void lds32B(uint32_t (&w)[8], uint32_t addr) {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any copy's latency
 
 // Geometry of the staged streaming kernels: a tile is kPipeCPT 32-byte chunks per thread
-// (16 KiB for 256 threads), kPipeStages tiles in flight per CTA.
-constexpr int kPipeCPT = 2;
+// (32 KiB for 256 threads), kPipeStages tiles in flight per CTA (64 KiB, 3 CTAs per SM).
+// Measured against 16 KiB tiles in 4 stages on a 32768 x 8192 bf16 tensor: fewer waits,
+// block synchronisations and refills per chunk made every staged kernel as fast or faster
+// (amax 84.6 -> 82.6 us, NVFP4 quantize with statistics 162 -> 156 us, INT4 166 -> 160 us).
+constexpr int kPipeCPT = 4;
 constexpr int kPipeTileChunks = kThreads * kPipeCPT;
 constexpr int kPipeTileBytes = kPipeTileChunks * 32;
-constexpr int kPipeStages = 4;
+constexpr int kPipeStages = 2;
 constexpr size_t kPipeSmem = static_cast<size_t>(kPipeStages) * kPipeTileBytes;
 
 // Streams the tiles of one CTA through S shared-memory stages.  Tile k of this CTA is

@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(kThreads) quant4_kernel(Q4Args a) {
 
 // ---------------------------------------------------------------------------------------
 // Dense tensors (rows back to back, 16-byte aligned): the input is streamed through shared
-// memory by 1-D bulk copies, 16 KiB per tile, 4 tiles in flight per CTA, so the memory
+// memory by 1-D bulk copies, 32 KiB per tile, 2 tiles in flight per CTA, so the memory
 // latency is covered by the pipeline instead of by registers.  The element arithmetic is
 // done on fp32 pairs (f32x2), which halves the FMA-pipe instructions, and the integer /
 // compare work is kept to 3-input max, the casts and the per-block scale.
@@ -202,13 +202,12 @@ __global__ void __launch_bounds__(kThreads) quant4_kernel(Q4Args a) {
 constexpr int kCPT = kPipeCPT;
 constexpr int kTileChunks = kPipeTileChunks;
 constexpr int kTileBytes = kPipeTileBytes;
-constexpr int kStages = kPipeStages;
-// tiles in flight and resident CTAs per SM of the staged quantizer, per format (measured:
-// MXFP4 gains from a fourth CTA with one stage less; NVFP4, at 72 registers, would spill)
+// tiles in flight and resident CTAs per SM of the staged quantizer (the same for both
+// formats since the 32 KiB tiles; with 16 KiB tiles MXFP4 had run 4 CTAs x 3 stages)
 template <int FMT>
 struct PipeShape {
-  static constexpr int kStages = FMT == QZ_MXFP4 ? 3 : kPipeStages;
-  static constexpr int kCtas = FMT == QZ_MXFP4 ? 4 : 3;
+  static constexpr int kStages = kPipeStages;
+  static constexpr int kCtas = 3;
 };
 
 // Largest magnitude of 2*NP values held as fp32 pairs, as a tree of 3-input maxima (short

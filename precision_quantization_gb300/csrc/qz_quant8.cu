@@ -373,8 +373,8 @@ __device__ __forceinline__ void q8_chunk(const uint32_t (&w)[8], bool valid, uin
   }
 }
 
-// Dense tensors, per-tensor or unit scale: the quant4 pipeline (16 KiB tiles streamed
-// through shared memory by bulk copies, two 32-byte chunks per lane per tile).
+// Dense tensors, per-tensor or unit scale: the quant4 pipeline (32 KiB tiles streamed
+// through shared memory by bulk copies, four 32-byte chunks per lane per tile).
 template <int FMT, int DT, int MODE, bool STATS>
 __global__ void __launch_bounds__(kThreads, 3) quant8_pipe_kernel(Q8Args a, float zero) {
   constexpr int EPC = Elem<DT>::kPer32B;
