@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 3) int4_pipe_kernel(I4Args a, float 
     if (!P.wait(k)) s_abort = 1;
     float tpart = 0.0f;
     const uint32_t stage = P.stage(k);
-#pragma unroll
+#pragma unroll 1  // not unrolled: a smaller loop body (measured 160 -> 152 us, 32768 x 8192 bf16)
     for (int c = 0; c < kPipeCPT; ++c) {
       const int j = c * kThreads + tid;
       const int64_t u = tile * kPipeTileChunks + j;

@@ -438,7 +438,9 @@ __global__ void __launch_bounds__(kThreads, PipeShape<FMT>::kCtas) quant4_pipe_k
     if (!P.wait(k)) s_abort = 1;
     float tpart = 0.0f;  // in-range chunk sums of squares of this tile
     const uint32_t stage = P.stage(k);
-#pragma unroll
+    // not unrolled: one copy of the chunk code per REL variant keeps the loop body small
+    // (measured 1-2 us faster than unrolled on a 32768 x 8192 bf16 tensor)
+#pragma unroll 1
     for (int c = 0; c < kCPT; ++c) {
       const int j = c * kThreads + tid;
       const int64_t u = tile * kTileChunks + j;  // global 32-byte chunk
