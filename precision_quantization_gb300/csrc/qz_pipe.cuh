@@ -82,6 +82,25 @@ __device__ __forceinline__ uint64_t widen_bf16x2(uint32_t w) {
   return pk(lo, hi);
 }
 
+// Largest |x| of the 16 bf16 values in w[0..7], NaN propagating: a tree of packed
+// bf16x2 maxima of magnitudes (the sign of each partial result is immaterial), then the
+// two halves of the last word widened (exactly) and compared.
+__device__ __forceinline__ float bf16x16_absmax(const uint32_t (&w)[8]) {
+  uint32_t m0, m1, m2, m3;
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m0) : "r"(w[0]), "r"(w[1]));
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m1) : "r"(w[2]), "r"(w[3]));
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m2) : "r"(w[4]), "r"(w[5]));
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(m3) : "r"(w[6]), "r"(w[7]));
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m0) : "r"(m1));
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m2) : "r"(m3));
+  asm("max.NaN.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m0) : "r"(m2));
+  float lo, hi;
+  upk(widen_bf16x2(m0), lo, hi);
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(fabsf(lo)), "f"(fabsf(hi)));
+  return d;
+}
+
 // Eight quotients -> one 32-bit word of E2M1 codes (element 0 in bits [0,4)) and the
 // decoded code values as four f16x2 words.
 __device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8], uint32_t (&h)[4]) {

@@ -254,7 +254,7 @@ struct Q4Ctx {
 // One 32-byte chunk: block amax, scale, quotients, cast, stores, and (STATS) the error of
 // the chunk.  REL: the exact max |e|/|x| search is still open for this warp (T < 1).
 // am: running max of the block amaxes' bits (the tensor amax, for amax_out).
-template <int FMT, int DT, bool UNIT, bool STATS, int SR, bool REL>
+template <int FMT, int DT, bool UNIT, bool STATS, int SR, bool REL, bool AMAX>
 __device__ __forceinline__ void q4_chunk(const Q4Args& a, const Q4Ctx& cx, const uint32_t (&w)[8],
                                          int64_t u, bool valid, int lane, StatAcc& acc,
                                          float& tpart, uint32_t& am) {
@@ -269,11 +269,16 @@ __device__ __forceinline__ void q4_chunk(const Q4Args& a, const Q4Ctx& cx, const
     if constexpr (DT == QZ_BF16) xp[p] = widen_bf16x2(w[p]);
     else xp[p] = pk(__uint_as_float(w[2 * p]), __uint_as_float(w[2 * p + 1]));
   }
-  float A = pairs_absmax<NP, true>(xp);
+  float A;
+  if constexpr (DT == QZ_BF16) A = bf16x16_absmax(w);  // packed bf16x2 maxima: fewer ALU slots
+  else A = pairs_absmax<NP, true>(xp);
   if constexpr (L >= 2) A = absmax_nan(A, __shfl_xor_sync(kFull, A, 1));
   if constexpr (L >= 4) A = absmax_nan(A, __shfl_xor_sync(kFull, A, 2));
-  if (valid && !is_finite_f(A)) flag_status(a.ws, QZ_FLAG_NONFINITE_INPUT);
-  am = max(am, __float_as_uint(A));  // A >= 0; lanes without data hold 0
+  // A NaN / Inf block amax is flagged here for UNIT and MXFP4 NEAREST; the MXFP4 UP and
+  // NVFP4 scale paths send it to their out-of-line branch and flag it there
+  constexpr bool kFlagHere = UNIT || (FMT == QZ_MXFP4 && SR != QZ_SCALE_UP);
+  if (kFlagHere && valid && !is_finite_f(A)) flag_status(a.ws, QZ_FLAG_NONFINITE_INPUT);
+  if constexpr (AMAX) am = max(am, __float_as_uint(A));  // A >= 0; lanes without data hold 0
 
   // block scale s and the quotients v = fl32(x / s), as fp32 pairs
   uint32_t scode;
@@ -291,7 +296,10 @@ __device__ __forceinline__ void q4_chunk(const Q4Args& a, const Q4Ctx& cx, const
       // normal (A >= 2^-123).  A = 0 gives -129, clamped to -127.
       const uint32_t b = __float_as_uint(A);
       kexp = max(-127, static_cast<int>(b >> 23) - 129 + ((b & 0x7fffffu) > 0x400000u ? 1 : 0));
-      if (b - 1u < 0x01ffffffu || b >= 0x7f800000u) kexp = mx_exponent(div6(A), SR);
+      if (b - 1u < 0x01ffffffu || b >= 0x7f800000u) {  // tiny, zero-adjacent or NaN / Inf
+        if (valid && b >= 0x7f800000u) flag_status(a.ws, QZ_FLAG_NONFINITE_INPUT);
+        kexp = mx_exponent(div6(A), SR);
+      }
     } else {
       kexp = mx_exponent(div6(A), SR);
     }
@@ -318,6 +326,8 @@ __device__ __forceinline__ void q4_chunk(const Q4Args& a, const Q4Ctx& cx, const
       const uint32_t tb = __float_as_uint(t);
       const bool near = ((tb + 8u) & kMask) < 16u;
       if (!cx.c6_ok || near || (A != 0.0f && !(A >= 0x1p-100f && t >= 0x1p-100f))) {
+        // NaN fails the range test and +Inf makes t' = Inf, whose fraction field is "near"
+        if (valid && !is_finite_f(A)) flag_status(a.ws, QZ_FLAG_NONFINITE_INPUT);
         const float a6 = div6(A);  // (block_amax / 6) / s_global
         if (a6 >= 0x1p-100f && cx.sg_fast) {
           t = div_pos(a6, cx.sg, cx.rg);
@@ -391,7 +401,7 @@ __device__ __forceinline__ void q4_chunk(const Q4Args& a, const Q4Ctx& cx, const
   acc_pairs<NP, REL>(acc, xp, e, tpart);
 }
 
-template <int FMT, int DT, bool UNIT, bool STATS, int SR>
+template <int FMT, int DT, bool UNIT, bool STATS, int SR, bool AMAX>
 __global__ void __launch_bounds__(kThreads, PipeShape<FMT>::kCtas) quant4_pipe_kernel(Q4Args a) {
   constexpr int S = PipeShape<FMT>::kStages;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -453,9 +463,9 @@ __global__ void __launch_bounds__(kThreads, PipeShape<FMT>::kCtas) quant4_pipe_k
         for (int i = 0; i < 8; ++i) w[i] = 0u;
       }
       if (!STATS || acc.T >= 1.0f)  // warp-uniform: the relative-error search is settled
-        q4_chunk<FMT, DT, UNIT, STATS, SR, false>(a, cx, w, u, valid, lane, acc, tpart, am);
+        q4_chunk<FMT, DT, UNIT, STATS, SR, false, AMAX>(a, cx, w, u, valid, lane, acc, tpart, am);
       else
-        q4_chunk<FMT, DT, UNIT, STATS, SR, true>(a, cx, w, u, valid, lane, acc, tpart, am);
+        q4_chunk<FMT, DT, UNIT, STATS, SR, true, AMAX>(a, cx, w, u, valid, lane, acc, tpart, am);
     }
     if constexpr (STATS) acc_add_sum(acc, tpart);
     __syncthreads();  // every thread is done with this stage
@@ -468,14 +478,14 @@ __global__ void __launch_bounds__(kThreads, PipeShape<FMT>::kCtas) quant4_pipe_k
     }
     if (tid == 0) P.issue(k + S);
   }
-  if (a.amax_out) amax_finish<QZ_F32>(am, a.amax_out, a.ws);
+  if constexpr (AMAX) amax_finish<QZ_F32>(am, a.amax_out, a.ws);
   if constexpr (STATS) stats_finish(acc, a.ws, a.stats, static_cast<uint64_t>(a.g.rows * a.g.cols));
 }
 
-template <int FMT, int DT, bool UNIT, bool STATS>
-qz_status run_pipe(const Q4Args& args, cudaStream_t s) {
-  auto kern = args.scale_round == QZ_SCALE_NEAREST ? &quant4_pipe_kernel<FMT, DT, UNIT, STATS, QZ_SCALE_NEAREST>
-                                                    : &quant4_pipe_kernel<FMT, DT, UNIT, STATS, QZ_SCALE_UP>;
+template <int FMT, int DT, bool UNIT, bool STATS, bool AMAX>
+qz_status run_pipe_k(const Q4Args& args, cudaStream_t s) {
+  auto kern = args.scale_round == QZ_SCALE_NEAREST ? &quant4_pipe_kernel<FMT, DT, UNIT, STATS, QZ_SCALE_NEAREST, AMAX>
+                                                    : &quant4_pipe_kernel<FMT, DT, UNIT, STATS, QZ_SCALE_UP, AMAX>;
   constexpr size_t smem = static_cast<size_t>(PipeShape<FMT>::kStages) * kTileBytes;
   if (!set_dyn_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem)))
     return QZ_ERR_CUDA;
@@ -483,6 +493,13 @@ qz_status run_pipe(const Q4Args& args, cudaStream_t s) {
                             (args.g.n_chunks + kTileChunks - 1) / kTileChunks, s, smem);
   kern<<<grid, kThreads, smem, s>>>(args);
   return launch_status();
+}
+
+// AMAX: also fold this tensor's amax into amax_out (the delayed-scaling call)
+template <int FMT, int DT, bool UNIT, bool STATS>
+qz_status run_pipe(const Q4Args& args, cudaStream_t s) {
+  return args.amax_out ? run_pipe_k<FMT, DT, UNIT, STATS, true>(args, s)
+                       : run_pipe_k<FMT, DT, UNIT, STATS, false>(args, s);
 }
 
 // With amax_out, the staged kernel folds the tensor amax in; the direct path leaves it to

@@ -8,7 +8,7 @@ import pytest
 
 import oracle as O
 import workloads as W
-from gpu_util import assert_parity, run_gpu, run_oracle, to_device
+from gpu_util import assert_parity, run_gpu, run_oracle, to_device, torch_mod
 
 pytestmark = pytest.mark.gpu
 
@@ -169,6 +169,35 @@ def test_nonfinite_input_sets_status():
         assert ws.status() & qz.QZ_FLAG_NONFINITE_INPUT, (fmt, gran)
         ws.clear()
         assert ws.status() == 0
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("bad", [float("nan"), float("inf"), float("-inf")])
+@pytest.mark.parametrize("fmt,gran,sr", [(O.NVFP4, O.GRAN_BLOCK, O.SCALE_UP),
+                                         (O.NVFP4, O.GRAN_BLOCK, O.SCALE_NEAREST),
+                                         (O.MXFP4, O.GRAN_BLOCK, O.SCALE_UP),
+                                         (O.MXFP4, O.GRAN_BLOCK, O.SCALE_NEAREST),
+                                         (O.NVFP4, O.GRAN_UNIT, O.SCALE_UP),
+                                         (O.MXFP4, O.GRAN_UNIT, O.SCALE_UP)])
+def test_fp4_quantize_flags_nonfinite_itself(fmt, gran, sr, bad, dtype):
+    """One NaN or +-Inf element, the NVFP4 tensor amax supplied (finite), so no amax pass
+    runs: the FP4 quantize kernel must raise the flag itself, with and without the fused
+    statistics, and on the delayed path."""
+    import precision_quantization_gb300 as qz
+    torch = torch_mod()
+    x = torch.ones((64, 256), dtype=torch.float32, device="cuda")
+    x[17, 100] = bad
+    if dtype == "bf16":
+        x = x.to(torch.bfloat16)
+    alpha = torch.ones((1,), dtype=torch.float32, device="cuda")
+    ta = alpha if (fmt == O.NVFP4 and gran == O.GRAN_BLOCK) else None
+    for stats in (True, False):
+        ws = qz.Workspace()
+        qz.quantize(x, fmt, gran, sr, tensor_amax=ta, stats=stats, workspace=ws)
+        assert ws.status() & qz.QZ_FLAG_NONFINITE_INPUT, (fmt, gran, sr, bad, stats)
+    ws = qz.Workspace()
+    qz.quantize_delayed(x, fmt, ta, gran, sr, stats=True, workspace=ws)
+    assert ws.status() & qz.QZ_FLAG_NONFINITE_INPUT, (fmt, gran, sr, bad, "delayed")
 
 
 def test_bad_supplied_amax_sets_status():
