@@ -286,6 +286,7 @@ __device__ __forceinline__ void q4_chunk(const Q4Args& a, const Q4Ctx& cx, const
   uint64_t vp[NP];
   bool mul_exact = false;  // MXFP4: decode(q) * 2^k exact, so e = fma(-q, s, x)
   int kexp = 0;
+  float inv = 1.0f;        // MXFP4: 2^-k
   if constexpr (FMT == QZ_MXFP4) {
     if constexpr (UNIT) {
       kexp = 0;
@@ -293,19 +294,31 @@ __device__ __forceinline__ void q4_chunk(const Q4Args& a, const Q4Ctx& cx, const
       // With A = m * 2^e (m in [1,2)), A/6 = (m/1.5) * 2^(e-2): fl32(A/6) <= 2^(e-2) exactly
       // when m <= 1.5, and lies in (2^(e-2), 2^(e-1)) otherwise, so the smallest k with
       // 2^k >= fl32(A/6) is e - 2 + [m > 1.5] -- read off A's fields, valid while A/6 is
-      // normal (A >= 2^-123).  A = 0 gives -129, clamped to -127.
+      // normal.  The [m > 1.5] is the carry of the fraction field plus (2^22 - 1) into the
+      // exponent field, so the code k + 127 is ((bits + 2^22 - 1) >> 23) - 2, in [2, 253]
+      // for A in [2^-125, 2^128); there s = 2^k and 1/s are plain exponent fields.  Zero,
+      // tiny and non-finite A take the general route.
       const uint32_t b = __float_as_uint(A);
-      kexp = max(-127, static_cast<int>(b >> 23) - 129 + ((b & 0x7fffffu) > 0x400000u ? 1 : 0));
-      if (b - 1u < 0x01ffffffu || b >= 0x7f800000u) {  // tiny, zero-adjacent or NaN / Inf
+      if (b - 0x02000000u < 0x7d800000u) {
+        scode = ((b + 0x3fffffu) >> 23) - 2u;
+        kexp = static_cast<int>(scode) - 127;
+        s = __uint_as_float(scode << 23);
+        inv = __uint_as_float((254u - scode) << 23);
+      } else {
         if (valid && b >= 0x7f800000u) flag_status(a.ws, QZ_FLAG_NONFINITE_INPUT);
         kexp = mx_exponent(div6(A), SR);
+        scode = static_cast<uint32_t>(kexp + 127);
+        s = exp2_pos(kexp);
+        inv = exp2_neg(kexp);
       }
     } else {
       kexp = mx_exponent(div6(A), SR);
     }
-    scode = static_cast<uint32_t>(kexp + 127);
-    s = exp2_pos(kexp);
-    const float inv = exp2_neg(kexp);
+    if constexpr (UNIT || SR != QZ_SCALE_UP) {
+      scode = static_cast<uint32_t>(kexp + 127);
+      s = exp2_pos(kexp);
+      inv = exp2_neg(kexp);
+    }
     const uint64_t inv2 = pk(inv, inv);
 #pragma unroll
     for (int p = 0; p < NP; ++p) vp[p] = mul2(xp[p], inv2);
