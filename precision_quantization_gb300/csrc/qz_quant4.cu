@@ -287,6 +287,7 @@ __device__ __forceinline__ void q4_chunk(const Q4Args& a, const Q4Ctx& cx, const
   bool mul_exact = false;  // MXFP4: decode(q) * 2^k exact, so e = fma(-q, s, x)
   int kexp = 0;
   float inv = 1.0f;        // MXFP4: 2^-k
+  float nv_ns = 0.0f;      // NVFP4: -s
   if constexpr (FMT == QZ_MXFP4) {
     if constexpr (UNIT) {
       kexp = 0;
@@ -351,13 +352,14 @@ __device__ __forceinline__ void q4_chunk(const Q4Args& a, const Q4Ctx& cx, const
       }
       scode = nv_block_code(t, SR);
     }
-    const float2 sr = cx.tab[scode];
-    s = sr.x;
+    const float2 sr = cx.tab[scode];  // (-s, RN(1/s))
+    s = -sr.x;
+    nv_ns = sr.x;
     if (UNIT) {  // s = 1: fl32(x / 1) = x
 #pragma unroll
       for (int p = 0; p < NP; ++p) vp[p] = xp[p];
-    } else if (sr.y != 0.0f && __fmul_rn(A, sr.y) <= 0x1p126f) {
-      const uint64_t r2 = pk(sr.y, sr.y), ns2 = pk(-s, -s);
+    } else if (__fmul_rn(A, sr.y) <= 0x1p126f) {  // NaN 1/s (no exact FMA quotient) fails
+      const uint64_t r2 = pk(sr.y, sr.y), ns2 = pk(sr.x, sr.x);
 #pragma unroll
       for (int p = 0; p < NP; ++p) vp[p] = div2(xp[p], r2, ns2);
     } else if (s == 0.0f) {
@@ -407,9 +409,11 @@ __device__ __forceinline__ void q4_chunk(const Q4Args& a, const Q4Ctx& cx, const
 #pragma unroll
     for (int p = 0; p < NP; ++p) e.v[p] = fma2(f16x2_to_f32x2(h[p / 4][p % 4]), ns2, xp[p]);
   } else {
-    const uint64_t s2 = pk(s, s), z2 = pk(cx.zero, cx.zero);
+    // x + fl32(q * -s) = x - fl32(q * s)
+    const float ns = FMT == QZ_NVFP4 ? nv_ns : -s;
+    const uint64_t ns2 = pk(ns, ns), z2 = pk(cx.zero, cx.zero);
 #pragma unroll
-    for (int p = 0; p < NP; ++p) e.v[p] = sub2(xp[p], mul2_rounded(f16x2_to_f32x2(h[p / 4][p % 4]), s2, z2));
+    for (int p = 0; p < NP; ++p) e.v[p] = add2(xp[p], mul2_rounded(f16x2_to_f32x2(h[p / 4][p % 4]), ns2, z2));
   }
   acc_pairs<NP, REL>(acc, xp, e, tpart);
 }
@@ -419,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, PipeShape<FMT>::kCtas) quant4_pipe_k
   constexpr int S = PipeShape<FMT>::kStages;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t bars[S];
-  __shared__ float2 tab[128];  // NVFP4: (s, RN(1/s)) for every E4M3 block code
+  __shared__ float2 tab[128];  // NVFP4: (-s, RN(1/s)) for every E4M3 block code; NaN 1/s: divide
   __shared__ int s_abort;
   const int tid = threadIdx.x, lane = tid & 31;
   const int64_t n_chunks = a.g.n_chunks;
@@ -439,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, PipeShape<FMT>::kCtas) quant4_pipe_k
     cx.c6 = __frcp_rn(__fmul_rn(6.0f, cx.sg));
     for (int c = tid; c < 128; c += kThreads) {
       const float s = __fmul_rn(cx.sg, dec_e4m3(static_cast<uint32_t>(c)));
-      tab[c] = make_float2(s, (s > 0.0f && fast_div_ok(s)) ? __frcp_rn(s) : 0.0f);
+      tab[c] = make_float2(-s, (s > 0.0f && fast_div_ok(s)) ? __frcp_rn(s) : __uint_as_float(0x7fc00000u));
     }
   }
   if (a.tscale_out && blockIdx.x == 0 && tid == 0) *a.tscale_out = cx.sg;
