@@ -191,27 +191,32 @@ __device__ __forceinline__ void i4_chunk(const I4Args& a, const uint32_t (&w)[8]
     if constexpr (DT == QZ_BF16) xp[p] = widen_bf16x2(w[p]);
     else xp[p] = pk(__uint_as_float(w[2 * p]), __uint_as_float(w[2 * p + 1]));
   }
-  float A = 0.0f;
+  float A;
+  if constexpr (DT == QZ_BF16) {
+    A = bf16x16_absmax(w);  // packed bf16x2 maxima: fewer ALU slots than fp32 maxima
+  } else {
+    A = 0.0f;
 #pragma unroll
-  for (int p = 0; p < NP; ++p) {
-    float x0, x1;
-    upk(xp[p], x0, x1);
-    A = absmax3(A, x0, x1);
+    for (int p = 0; p < NP; ++p) {
+      float x0, x1;
+      upk(xp[p], x0, x1);
+      A = absmax3(A, x0, x1);
+    }
   }
 #pragma unroll
   for (int o = 1; o < L; o <<= 1) A = absmax_nan(A, __shfl_xor_sync(kFull, A, o));
-  if (valid && !is_finite_f(A)) flag_status(a.ws, QZ_FLAG_NONFINITE_INPUT);
 
   float s = div7(A);
   if (s == 0.0f) s = 1.0f;
   const float r = __frcp_rn(s);
   const bool fast = fast_div_ok(s) && __fmul_rn(A, r) <= 0x1p126f;
   uint64_t vp[NP];
-  if (__all_sync(kFull, fast)) {
+  if (__all_sync(kFull, fast)) {  // a NaN / Inf amax makes s non-finite: never fast
     const uint64_t r2 = pk(r, r), ns2 = pk(-s, -s);
 #pragma unroll
     for (int p = 0; p < NP; ++p) vp[p] = div2(xp[p], r2, ns2);
   } else {
+    if (valid && !is_finite_f(A)) flag_status(a.ws, QZ_FLAG_NONFINITE_INPUT);
 #pragma unroll
     for (int p = 0; p < NP; ++p) {
       float x0, x1;

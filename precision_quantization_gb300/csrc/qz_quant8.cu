@@ -304,7 +304,7 @@ __device__ __forceinline__ void q8_cast(const uint64_t (&vp)[NP], uint32_t (&cw)
 
 // One chunk of the per-tensor / unit-scale path: quotients, cast, store, stats.  am: running
 // max of the chunk amaxes' bits (MODE != kTensorComputed; the tensor amax for amax_out).
-template <int FMT, int DT, int MODE, bool STATS, bool REL>
+template <int FMT, int DT, int MODE, bool STATS, bool REL, bool AMAX = true>
 __device__ __forceinline__ void q8_chunk(const uint32_t (&w)[8], bool valid, uint8_t* cp, float s,
                                          uint64_t r2, uint64_t ns2, uint64_t s2, uint64_t z2, bool fast,
                                          void* ws, StatAcc& acc, float& tpart, uint32_t& am) {
@@ -320,19 +320,27 @@ __device__ __forceinline__ void q8_chunk(const uint32_t (&w)[8], bool valid, uin
   if constexpr (MODE != kTensorComputed) {
     // no earlier pass has looked at these values: check finiteness here, and keep the FMA
     // quotient only where |x| / s cannot overflow (a supplied amax may be too small)
-    float A = 0.0f;
+    float A;
+    if constexpr (DT == QZ_BF16) {
+      A = bf16x16_absmax(w);  // packed bf16x2 maxima: fewer ALU slots than fp32 maxima
+    } else {
+      A = 0.0f;
 #pragma unroll
-    for (int p = 0; p < NP; ++p) {
-      float a, b;
-      upk(xp[p], a, b);
-      A = absmax3(A, a, b);
+      for (int p = 0; p < NP; ++p) {
+        float a, b;
+        upk(xp[p], a, b);
+        A = absmax3(A, a, b);
+      }
     }
-    if (valid && !is_finite_f(A)) flag_status(ws, QZ_FLAG_NONFINITE_INPUT);
-    am = max(am, __float_as_uint(A));
+    // UNIT checks finiteness here; with a supplied scale a NaN / Inf A fails the quotient
+    // range test and is flagged on the division path below
+    if (MODE == kUnit && valid && !is_finite_f(A)) flag_status(ws, QZ_FLAG_NONFINITE_INPUT);
+    if constexpr (AMAX) am = max(am, __float_as_uint(A));
     if constexpr (MODE == kTensorSupplied) {
       float r, rr;
       upk(r2, r, rr);
       f = f && (__fmul_rn(A, r) <= 0x1p126f);
+      if (!f && valid && !is_finite_f(A)) flag_status(ws, QZ_FLAG_NONFINITE_INPUT);
     }
   }
   uint64_t vp[NP];
@@ -375,7 +383,7 @@ __device__ __forceinline__ void q8_chunk(const uint32_t (&w)[8], bool valid, uin
 
 // Dense tensors, per-tensor or unit scale: the quant4 pipeline (32 KiB tiles streamed
 // through shared memory by bulk copies, four 32-byte chunks per lane per tile).
-template <int FMT, int DT, int MODE, bool STATS>
+template <int FMT, int DT, int MODE, bool STATS, bool AMAX>
 __global__ void __launch_bounds__(kThreads, 3) quant8_pipe_kernel(Q8Args a, float zero) {
   constexpr int EPC = Elem<DT>::kPer32B;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -429,9 +437,9 @@ __global__ void __launch_bounds__(kThreads, 3) quant8_pipe_kernel(Q8Args a, floa
       }
       uint8_t* cp = a.codes + u * EPC;
       if (!STATS || acc.T >= 1.0f)  // warp-uniform: the relative-error search is settled
-        q8_chunk<FMT, DT, MODE, STATS, false>(w, valid, cp, s, r2, ns2, s2, z2, fast, a.ws, acc, tpart, am);
+        q8_chunk<FMT, DT, MODE, STATS, false, AMAX>(w, valid, cp, s, r2, ns2, s2, z2, fast, a.ws, acc, tpart, am);
       else
-        q8_chunk<FMT, DT, MODE, STATS, true>(w, valid, cp, s, r2, ns2, s2, z2, fast, a.ws, acc, tpart, am);
+        q8_chunk<FMT, DT, MODE, STATS, true, AMAX>(w, valid, cp, s, r2, ns2, s2, z2, fast, a.ws, acc, tpart, am);
     }
     if constexpr (STATS) acc_add_sum(acc, tpart);
     __syncthreads();
@@ -445,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 3) quant8_pipe_kernel(Q8Args a, floa
     if (tid == 0) P.issue(k + kPipeStages);
   }
   if constexpr (MODE != kTensorComputed) {
-    if (a.amax_out) amax_finish<QZ_F32>(am, a.amax_out, a.ws);
+    if constexpr (AMAX) amax_finish<QZ_F32>(am, a.amax_out, a.ws);
   }
   if constexpr (STATS) stats_finish(acc, a.ws, a.stats, static_cast<uint64_t>(a.g.rows * a.g.cols));
 }
@@ -602,7 +610,9 @@ template <int FMT, int DT, int MODE, bool STATS>
 qz_status run_flat(const Q8Args& args, cudaStream_t s, bool& fused) {
   if (args.g.vec && args.g.dense && reinterpret_cast<uintptr_t>(args.x) % 16 == 0) {
     fused = MODE != kTensorComputed;
-    auto kern = &quant8_pipe_kernel<FMT, DT, MODE, STATS>;
+    // AMAX: also fold this tensor's amax into amax_out (the delayed-scaling call)
+    auto kern = args.amax_out ? &quant8_pipe_kernel<FMT, DT, MODE, STATS, true>
+                              : &quant8_pipe_kernel<FMT, DT, MODE, STATS, false>;
     if (!set_dyn_smem(reinterpret_cast<const void*>(kern), static_cast<int>(kPipeSmem)))
       return QZ_ERR_CUDA;
     const int grid = grid_for(reinterpret_cast<const void*>(kern),
