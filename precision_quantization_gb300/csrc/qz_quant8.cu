@@ -573,10 +573,88 @@ __global__ void __launch_bounds__(kThreads) quant8_rowpipe_kernel(Q8Args a, floa
   if constexpr (STATS) stats_finish(acc, a.ws, a.stats, static_cast<uint64_t>(g.rows * g.cols));
 }
 
+// Per-row scale with short rows (at most 32 * RCH chunks, full 32-byte chunks): one warp
+// per row.  Each lane loads its RCH chunks of the row with 256-bit loads into registers,
+// the row amax is a warp reduction (no block-wide synchronisation, so the warps of a CTA
+// run their rows independently and the per-row latency overlaps across warps), and the
+// codes come from the registers, so x is read once.
+template <int FMT, int DT, bool STATS, int RCH>
+__global__ void __launch_bounds__(kThreads) quant8_rowwarp_kernel(Q8Args a, float zero) {
+  constexpr int EPC = Elem<DT>::kPer32B;
+  const Geom& g = a.g;
+  const int lane = threadIdx.x & 31;
+  if (a.tscale_out && blockIdx.x == 0 && threadIdx.x == 0) *a.tscale_out = 1.0f;
+  const uint64_t z2 = pk(zero, zero);
+  StatAcc acc;
+  uint32_t am_unused = 0u;
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); row < g.rows;
+       row += nwarps) {  // warp-uniform
+    const char* xrow = static_cast<const char*>(a.x) + row * g.ld * Elem<DT>::kBytes;
+    uint32_t w[RCH][8];
+    float A = 0.0f;
+#pragma unroll
+    for (int k = 0; k < RCH; ++k) {
+      const int64_t j = lane + 32 * k;
+      if (j < g.cpr) {
+        ld32B(w[k], xrow + j * 32);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[k][i] = 0u;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < RCH; ++k) {
+      if constexpr (DT == QZ_BF16) {
+        A = absmax_nan(A, bf16x16_absmax(w[k]));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) A = absmax3(A, __uint_as_float(w[k][i]), __uint_as_float(w[k][i + 1]));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) A = absmax_nan(A, __shfl_xor_sync(kFull, A, o));
+    float s = __fdiv_rn(A, Fmt8<FMT>::kMax);  // alpha / qmax
+    if (s == 0.0f) s = 1.0f;
+    const float r = __frcp_rn(s);
+    const bool fast = fast_div_ok(s);
+    if (lane == 0) {
+      a.scales[row] = s;
+      if (!is_finite_f(A)) flag_status(a.ws, QZ_FLAG_NONFINITE_INPUT);
+    }
+    const uint64_t r2 = pk(r, r), ns2 = pk(-s, -s), s2 = pk(s, s);
+    float tpart = 0.0f;
+    uint8_t* crow = a.codes + row * g.cols;
+#pragma unroll
+    for (int k = 0; k < RCH; ++k) {
+      if (32 * k < g.cpr) {  // warp-uniform
+        const int64_t j = lane + 32 * k;
+        if (!STATS || acc.T >= 1.0f)
+          q8_chunk<FMT, DT, kTensorComputed, STATS, false, false>(w[k], j < g.cpr, crow + j * EPC, s, r2,
+                                                                  ns2, s2, z2, fast, a.ws, acc, tpart,
+                                                                  am_unused);
+        else
+          q8_chunk<FMT, DT, kTensorComputed, STATS, true, false>(w[k], j < g.cpr, crow + j * EPC, s, r2,
+                                                                 ns2, s2, z2, fast, a.ws, acc, tpart,
+                                                                 am_unused);
+      }
+    }
+    if constexpr (STATS) acc_add_sum(acc, tpart);
+  }
+  if constexpr (STATS) stats_finish(acc, a.ws, a.stats, static_cast<uint64_t>(g.rows * g.cols));
+}
+
 template <typename K>
 qz_status go(K kern, const Q8Args& args, int64_t work_ctas, cudaStream_t s) {
   const int grid = grid_for(reinterpret_cast<const void*>(kern), work_ctas, s);
   kern<<<grid, kThreads, 0, s>>>(args);
+  return launch_status();
+}
+
+template <typename K>
+qz_status go2(K kern, const Q8Args& args, int64_t work_ctas, cudaStream_t s) {  // (args, 0.0f) kernels
+  const int grid = grid_for(reinterpret_cast<const void*>(kern), work_ctas, s);
+  kern<<<grid, kThreads, 0, s>>>(args, 0.0f);
   return launch_status();
 }
 
@@ -585,6 +663,17 @@ qz_status run_row(const Q8Args& args, cudaStream_t s) {
   const Geom& g = args.g;
   const int64_t rows = g.rows;
   const int64_t row_bytes = g.cols * Elem<DT>::kBytes;
+  // short rows of whole 32-byte chunks (vector path: aligned, cols a multiple of a chunk),
+  // without statistics: one warp per row, the row in registers.  (With statistics the
+  // row pipeline below measured faster on the weight-like rows: 8 unrolled chunks per lane,
+  // each in two variants of the relative-error search, make a large loop body.)
+  if (!STATS && g.vec && g.cpr <= 256 && reinterpret_cast<uintptr_t>(args.x) % 32 == 0 &&
+      (g.ld * Elem<DT>::kBytes) % 32 == 0 && g.cols % Elem<DT>::kPer32B == 0) {
+    const int64_t work = (rows + kWarps - 1) / kWarps;
+    if (g.cpr <= 64) return go2(&quant8_rowwarp_kernel<FMT, DT, STATS, 2>, args, work, s);
+    if (g.cpr <= 128) return go2(&quant8_rowwarp_kernel<FMT, DT, STATS, 4>, args, work, s);
+    return go2(&quant8_rowwarp_kernel<FMT, DT, STATS, 8>, args, work, s);
+  }
   if (g.vec && row_bytes <= kRowPipeMaxBytes && reinterpret_cast<uintptr_t>(args.x) % 16 == 0 &&
       (g.ld * Elem<DT>::kBytes) % 16 == 0) {
     auto kern = &quant8_rowpipe_kernel<FMT, DT, STATS>;

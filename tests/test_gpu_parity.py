@@ -63,6 +63,19 @@ def test_parity_strided_rows(fmt, gran, dtype, pad):
     assert_parity(run_gpu(x, fmt, gran, ld_pad=pad), run_oracle(x, fmt, gran))
 
 
+@pytest.mark.parametrize("kind", ["lognormal", "edge"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("fmt", FMT8)
+def test_parity_row_without_stats(fmt, dtype, kind):
+    """Per-row scales without the fused statistics (short rows take a kernel of their
+    own there: a warp per row, 2 / 4 / 8 chunks per lane), including rows of one chunk,
+    ragged widths and rows too long for it."""
+    for i, (rows, cols) in enumerate(SHAPES8 + [(300, 2048), (1000, 512), (77, 4096 + 16)]):
+        x = gen(rows, cols, dtype, seed=700 + i, kind=kind)
+        assert_parity(run_gpu(x, fmt, O.GRAN_ROW, stats=False),
+                      run_oracle(x, fmt, O.GRAN_ROW, stats=False), stats=False)
+
+
 @pytest.mark.parametrize("fmt,gran", [(O.INT8, O.GRAN_TENSOR), (O.E4M3, O.GRAN_TENSOR),
                                       (O.E5M2, O.GRAN_TENSOR), (O.NVFP4, O.GRAN_BLOCK)])
 @pytest.mark.parametrize("factor", [1.0, 0.25, 4.0, 1e-30, 0.0])
@@ -298,3 +311,5 @@ def test_named_workload_full_size(k):
         o = run_oracle(x, fmt, gran, out_dtypes=od)
         assert_parity(g, o)
         assert g["status"] == 0
+        if gran == O.GRAN_ROW:  # the quantize without statistics runs other kernels there
+            assert_parity(run_gpu(x, fmt, gran, stats=False, out_dtypes=od), o, stats=False)
