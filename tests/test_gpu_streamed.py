@@ -72,6 +72,26 @@ def test_round_trip_reused_plan_f32_edge_mix():
             check_run(plan, j, x_np, f, g)
 
 
+def test_round_trip_without_stats():
+    """The plan without the fused statistics: the same codes, scales and dequantized values
+    (the NVFP4 and TENSOR formats still take their amax over all chunks)."""
+    from precision_quantization_gb300.streamed import HostRoundTrip
+    rows, cols = 513, 1024
+    x_np = W.activation_like(rows, cols, seed=71)
+    plan = HostRoundTrip(rows, cols, RUNS, chunk_rows=200, stats=False)
+    plan.run(host_tensor(x_np))
+    for j, (f, g) in enumerate(RUNS):
+        o = run_oracle(x_np, f, g, stats=False, out_dtypes=("bf16",))
+        h = plan.host[j]
+        assert np.array_equal(h["codes"].numpy(), o["codes"]), (f, g)
+        if o["scales"] is not None:
+            sc = h["scales"].numpy()
+            assert np.array_equal(sc.view(np.uint32) if sc.dtype == np.float32 else sc, o["scales"])
+        assert np.array_equal(to_host_bits(plan.y[j]), o["y"]["bf16"]), (f, g)
+    assert plan.bytes_out() == sum(t.numel() * t.element_size() for h in plan.host
+                                   for k, t in h.items() if t is not None and k != "stats")
+
+
 def test_round_trip_empty():
     from precision_quantization_gb300.streamed import HostRoundTrip
     torch = torch_mod()
