@@ -246,15 +246,21 @@ __device__ __forceinline__ void acc_pairs(StatAcc& acc, const uint64_t (&xp)[NP]
       else comp_add(acc.sS, acc.cS, ps);
     }
   }
-  if constexpr (REL) {  // see rel_candidate
-    bool cand = false;
+  if constexpr (REL) {
+    // An element can raise the maximum only if |e| > T |x|, and then (only then)
+    // fl32(T |x| - |e|) is negative or -0; such elements get the exact quotient
+    float d[2 * NP];
+    uint32_t sg = 0u;
 #pragma unroll
     for (int p = 0; p < NP; ++p) {
       float x0, x1, e0, e1;
       upk(xp[p], x0, x1);
       upk(e.v[p], e0, e1);
-      cand |= rel_candidate(acc.T, x0, fabsf(e0)) | rel_candidate(acc.T, x1, fabsf(e1));
+      d[2 * p] = __fmaf_rn(acc.T, fabsf(x0), -fabsf(e0));
+      d[2 * p + 1] = __fmaf_rn(acc.T, fabsf(x1), -fabsf(e1));
+      sg |= __float_as_uint(d[2 * p]) | __float_as_uint(d[2 * p + 1]);
     }
+    const bool cand = (sg & 0x80000000u) != 0u;
     if (__any_sync(kFull, cand)) {
       if (cand) {
 #pragma unroll
@@ -262,7 +268,8 @@ __device__ __forceinline__ void acc_pairs(StatAcc& acc, const uint64_t (&xp)[NP]
           float x0, x1, e0, e1;
           upk(xp[p], x0, x1);
           upk(e.v[p], e0, e1);
-          acc.rel = max3(acc.rel, rel_exact(x0, fabsf(e0)), rel_exact(x1, fabsf(e1)));
+          if (__float_as_uint(d[2 * p]) & 0x80000000u) acc.rel = fmaxf(acc.rel, rel_exact(x0, fabsf(e0)));
+          if (__float_as_uint(d[2 * p + 1]) & 0x80000000u) acc.rel = fmaxf(acc.rel, rel_exact(x1, fabsf(e1)));
         }
       }
       acc.T = warp_max(acc.rel);
