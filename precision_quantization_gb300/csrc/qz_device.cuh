@@ -355,12 +355,14 @@ __device__ __forceinline__ void acc_chunk(StatAcc& acc, const float (&xs)[N], co
   bool cand = false;
   const bool want_rel = acc.T < 1.0f;  // warp-uniform
   float e[N];
+  bool ci[N];       // element i can raise the maximum of |e| / |x|
   float cm = 0.0f;  // largest |e| of the chunk
 #pragma unroll
   for (int i = 0; i < N; ++i) {
     e[i] = __fsub_rn(xs[i], xh[i]);
     cm = fmaxf(cm, fabsf(e[i]));
-    if (want_rel) cand |= rel_candidate(acc.T, xs[i], fabsf(e[i]));
+    ci[i] = want_rel && rel_candidate(acc.T, xs[i], fabsf(e[i]));
+    cand |= ci[i];
   }
   acc.max_abs = fmaxf(acc.max_abs, cm);
   // the bucket of the chunk (see StatAcc): scale 1 for a largest |e| in [2^-40, 2^40] (or
@@ -378,9 +380,10 @@ __device__ __forceinline__ void acc_chunk(StatAcc& acc, const float (&xs)[N], co
   else if (cm > 0x1p40f) comp_add(acc.sL, acc.cL, part);
   else comp_add(acc.sS, acc.cS, part);
   if (want_rel && __any_sync(kFull, cand)) {
-    if (cand) {
+    if (cand) {  // the exact quotient for the candidates only
 #pragma unroll
-      for (int i = 0; i < N; ++i) acc.rel = fmaxf(acc.rel, rel_exact(xs[i], fabsf(e[i])));
+      for (int i = 0; i < N; ++i)
+        if (ci[i]) acc.rel = fmaxf(acc.rel, rel_exact(xs[i], fabsf(e[i])));
     }
     acc.T = warp_max(acc.rel);
   }
