@@ -152,9 +152,10 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# Every format of the five named workloads (workload 5: its first 4096 rows, 268 MB, to
-# bound the input generation time), timed per call: quantize with the fused error stats
-# (including the in-library amax pass where the scale is per tensor) and dequantize.
+# Every format of the five named workloads, all at full size, timed per call: quantize with
+# the fused error stats (including the in-library amax pass where the scale is per tensor),
+# the quantize alone, and dequantize; after an L2 flush (cold), and for the workloads that
+# fit the 126 MB L2 in part or whole (1 to 3) also back to back without it (warm).
 # "delayed": qz_quantize_delayed, the per-tensor scale from an amax handed in (here the
 # tensor's own, computed beforehand) and this tensor's amax returned, in one pass.
 MATRIX = [
@@ -171,6 +172,27 @@ MATRIX = [
 ]
 
 
+WARM_WORKLOADS = (1, 2, 3)
+
+
+def compact_matrix(rows: list) -> dict:
+    """One short string per matrix row, "q/qn/dq" fractions of the measured HBM peak
+    (quantize with statistics, quantize alone, dequantize; cold L2), then "|q/dq" warm for
+    the L2-sized workloads; kept at the end of the JSON line."""
+    def f(v):
+        return "-" if v is None else f"{v:.3f}".lstrip("0")
+    out = {}
+    for r in rows:
+        key = f"{r.get('workload_id', '?')}:{r['format']}/{r['granularity'].replace(' ', '')}"
+        v = f"{f(r.get('quantize_frac'))}/{f(r.get('quantize_nostats_frac'))}/{f(r.get('dequantize_frac'))}"
+        if "quantize_warm_frac" in r:
+            v += f"|{f(r['quantize_warm_frac'])}/{f(r['dequantize_warm_frac'])}"
+        if "tflops" in r:
+            v += f" {r['tflops']}TF/s={f(r['tflops_frac'])}"
+        out[key] = v
+    return out
+
+
 def measure_matrix(dev, peaks, flush, x4=None, reps=10, which=(1, 2, 3, 4, 5)) -> list:
     import numpy as np
     import torch
@@ -182,12 +204,13 @@ def measure_matrix(dev, peaks, flush, x4=None, reps=10, which=(1, 2, 3, 4, 5)) -
     ws = qz.Workspace(dev)
     st = torch.empty((qz.STATS_BYTES,), dtype=torch.uint8, device=dev)
 
-    def timed(fn):
+    def timed(fn, cold=True):
         for _ in range(3):
             fn()
         ts = []
         for _ in range(reps):
-            flush.zero_()
+            if cold:
+                flush.zero_()
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -218,10 +241,11 @@ def measure_matrix(dev, peaks, flush, x4=None, reps=10, which=(1, 2, 3, 4, 5)) -
         for run in runs:
             fname, gname = run[0], run[1]
             if fname == "asym4":
-                out.append(measure_asym4(name, r, c, run[2], timed, peaks, dev))
+                out.append({**measure_asym4(name, r, c, run[2], timed, peaks, dev), "workload_id": k})
                 continue
             if fname == "qdot":
-                out.append(measure_qdot(name, r, c, run[2], run[3], timed, peaks, dev))
+                out.append({**measure_qdot(name, r, c, run[2], run[3], timed, peaks, dev),
+                            "workload_id": k})
                 continue
             delayed = len(run) > 2 and run[2] == "delayed"
             bsz = run[2] if len(run) > 2 and isinstance(run[2], int) else None
@@ -251,7 +275,14 @@ def measure_matrix(dev, peaks, flush, x4=None, reps=10, which=(1, 2, 3, 4, 5)) -
             cb = codes.numel() + (0 if scales is None else scales.numel() * scales.element_size()) + 4
             qb = n * eb * (2 if amax_pass else 1) + cb + 32 + (8 if delayed else 0)
             db = cb + n * eb
-            out.append({"workload": name, "format": fname,
+            warm = {}
+            if k in WARM_WORKLOADS:
+                qw, dw = timed(lambda: q(st.data_ptr()), cold=False), timed(dq, cold=False)
+                warm = {"quantize_warm_us": round(qw * 1e3, 1),
+                        "quantize_warm_frac": round(qb / qw / 1e6 / peaks["hbm_gbs"], 3),
+                        "dequantize_warm_us": round(dw * 1e3, 1),
+                        "dequantize_warm_frac": round(db / dw / 1e6 / peaks["hbm_gbs"], 3)}
+            out.append({"workload": name, "workload_id": k, "format": fname,
                         "granularity": gname + (" delayed" if delayed else "") +
                                        (f" {bsz}" if bsz else ""),
                         "quantize_us": round(qms * 1e3, 1),
@@ -262,7 +293,7 @@ def measure_matrix(dev, peaks, flush, x4=None, reps=10, which=(1, 2, 3, 4, 5)) -
                         "quantize_nostats_frac": round(qb / qns / 1e6 / peaks["hbm_gbs"], 3),
                         "dequantize_us": round(dms * 1e3, 1),
                         "dequantize_gbs": round(db / dms / 1e6, 1),
-                        "dequantize_frac": round(db / dms / 1e6 / peaks["hbm_gbs"], 3)})
+                        "dequantize_frac": round(db / dms / 1e6 / peaks["hbm_gbs"], 3), **warm})
         del x
     if ws.status() != 0:
         raise RuntimeError("status flags set during the format matrix")
@@ -379,7 +410,53 @@ def cpu_baseline(x_np, bytes_per_elem: float, budget_s: float = 12.0, max_rows=N
     return {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": f"first {rows} rows x {x_np.shape[1]} of the workload ({n} elements), "
                       f"MXFP4+NVFP4 quantize(+stats)->dequantize, {dt:.2f} s",
-            "elements_per_s": round(n / dt, 1)}
+            "elements_per_s": round(n / dt, 1), **host_info(), "per_core": oracle_one_thread()}
+
+
+def host_info() -> dict:
+    """CPU model name (lscpu, else /proc/cpuinfo) and machine architecture of the host."""
+    import platform
+    model = None
+    try:
+        r = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10)
+        for ln in r.stdout.splitlines():
+            if ln.split(":")[0].strip() == "Model name":
+                model = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if model is None and os.path.exists("/proc/cpuinfo"):
+        with open("/proc/cpuinfo") as f:
+            for ln in f:
+                if ln.lower().startswith(("model name", "cpu part")):
+                    model = ln.split(":", 1)[1].strip()
+                    break
+    return {"cpu_model": model, "arch": platform.machine(), "nproc": os.cpu_count()}
+
+
+def oracle_one_thread() -> dict:
+    """The oracle on one thread over the whole small workload (1024 x 1024 bf16, N(0,1)):
+    every format of that workload quantized with statistics and dequantized to bf16 --
+    the per-core rate of the CPU baseline."""
+    import oracle as O
+    import workloads as W
+    x = W.workload(1)
+    n = x.size
+    runs = [(O.INT8, O.GRAN_TENSOR), (O.E4M3, O.GRAN_TENSOR), (O.MXFP4, O.GRAN_BLOCK),
+            (O.NVFP4, O.GRAN_BLOCK)]
+    nbytes = 0
+    t0 = time.perf_counter()
+    for fmt, gran in runs:
+        codes, sc, ts, _ = O.quantize(x, fmt, gran, stats=True, nthreads=1)
+        O.dequantize(codes, sc, ts, fmt, gran, x.shape[0], x.shape[1], out_dtype=O.BF16,
+                     nthreads=1)
+        out = codes.nbytes + (0 if sc is None else sc.nbytes) + 4
+        nbytes += 2 * (2 * n + out)  # quantize: x in, codes out; dequantize: codes in, y out
+    dt = time.perf_counter() - t0
+    return {"threads": 1, "workload": "normal-1024x1024-bf16",
+            "ops": "INT8, E4M3 (tensor), MXFP4, NVFP4: quantize(+stats) -> dequantize(bf16)",
+            "seconds": round(dt, 3), "gbs": round(nbytes / dt / 1e9, 4),
+            "elements_per_s": round(len(runs) * n / dt, 1)}
 
 
 def run_reference(args, world, rank):
@@ -641,13 +718,16 @@ def main():
                       "mse": stats_host[qz.QZ_NVFP4].mse,
                       "max_rel_err": stats_host[qz.QZ_NVFP4].max_rel_err},
         },
-        "formats": matrix,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": args.steps * len(names),
         "clocks": clk.summary(),
         "wall_s_timed_region": round(wall, 4),
     }
+    # the verbose matrix first and the compact one last: a reader that keeps only the end
+    # of the line still has every per-format cell
+    line = {"formats": matrix, **line}
+    line["format_fracs"] = None if matrix is None else compact_matrix(matrix)
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -209,22 +209,31 @@ QZ_API qz_status qz_error_stats(const qz_desc* desc, const void* x, const void* 
  * memory (code running under another framework's memory pool, paths on which cudaMalloc /
  * cudaFree and their device synchronisation are not allowed, plugins handed only their
  * input and output buffers).  The post has no counterpart; this is an interface matter.
- * Same arguments, results and errors as qz_error_stats otherwise.
+ * Same arguments, results and argument errors as qz_error_stats otherwise.
  *   Scratch: a fixed array of qz_workspace_size() bytes (82 176 in this version) in device
  *   memory, part of the library module: every GPU that loads the library holds it until
  *   the process exits.  The statistics need no more scratch for larger tensors; a
  *   descriptor whose workspace would exceed the array is rejected with QZ_ERR_WORKSPACE.
  *   Allocation: none -- no cudaMalloc, cudaFree or allocating library call.
  *   First call on a device: looks up the array's device address (cudaGetSymbolAddress,
- *   with that device current) and caches it; make that first call before any stream
- *   capture on the device.
+ *   with that device current) and caches it for the life of the device's context; make
+ *   that first call before any stream capture on the device, and do not use this entry
+ *   (or qz_error_stats_noalloc_status) across a cudaDeviceReset.
+ *   Status: a NaN / Inf element sets QZ_FLAG_NONFINITE_INPUT in the array's status word,
+ *   which keeps collecting flags until qz_error_stats_noalloc_status reads and clears it.
  *   Sharing: every call on a device uses the same array, which keeps what the previous
- *   call left; each call clears its counters behind its kernel on `stream`.  Calls that
- *   overlap on the GPU (different streams, no ordering between them) race on the array and
- *   give wrong statistics. */
+ *   call left (its completion counters return to 0 at the end of each call's kernel).
+ *   Calls that overlap on the GPU (different streams, no ordering between them) race on
+ *   the array and give wrong statistics. */
 QZ_API qz_status qz_error_stats_noalloc(const qz_desc* desc, const void* x, const void* codes,
                                         const void* scales, const float* tensor_scale_dev,
                                         qz_stats* stats_dev, qz_stream_t stream);
+
+/* Status flags (QZ_FLAG_* bits) that qz_error_stats_noalloc calls on the current device have
+ * raised since the last call of this function, read into *flags_host and cleared, both in
+ * order on `stream` behind the calls already enqueued there; then synchronizes `stream`.
+ * Allocates nothing.  The post has no counterpart; an interface matter. */
+QZ_API qz_status qz_error_stats_noalloc_status(uint32_t* flags_host, qz_stream_t stream);
 
 /* Statistics of one tensor from the statistics of its parts: `parts` holds `count` records
  * (device, 8-byte aligned) written by qz_quantize / qz_error_stats over disjoint parts of
@@ -259,9 +268,19 @@ QZ_API qz_status qz_dequantize_asym4(const uint32_t* w, const float* scales,
  *                      n0, cols = mid): each weight is fl32(sc * (w - sh)), as that call writes
  *   y                  device, bf16 activations [mid, ld_y], ld_y >= n1, 2-byte aligned
  *   z                  device, fp32 [n0, ld_z], ld_z >= n1, 4-byte aligned
- * The sum runs in fp32 in an unspecified order -- with group % 16 == 0 on the tensor cores
- * as sum over groups of sc * sum (w - sh) y, whose integer factors are exact in bf16 --
- * and every z[j][k] is within (2 mid + 8) * 2^-24 * sum_l |weight * y| of the exact sum.
+ * The sum runs in fp32 in an unspecified order.  With group % 16 == 0 it runs on the tensor
+ * cores as sum over groups of sc * sum (w - sh) y: the integer factors w - sh are exact in
+ * bf16, every product (w - sh) y is exact in fp32, and the scale is applied by one fp32 FMA
+ * per output and group.  Every z[j][k] is within
+ *     E * 2^-24 * sum_l |weight * y|,   E = 34 ceil(min(group, 1024) / 16) + ceil(mid / 32)
+ *                                            + ceil(mid / 256) + 24
+ * of the exact sum.  The 34 per 16 terms covers one tensor-core step c + sum of 16 exact
+ * products whose addends are aligned to the largest one and cut to 24 bits (truncation)
+ * and whose result is normalised with at most one more ulp: 16 addends lose under one ulp
+ * of the largest each, 2^-23 = 2 * 2^-24 relative, and the normalisation two more.  The
+ * other terms count the remaining fp32 roundings of the order used: one per weight
+ * rounding, one per group FMA, one per partial sum of split rows (FMA form: one per term a
+ * lane accumulates, mid / 32 at most, five in the warp reduction).
  * n1 in [1, 8] (few activation columns: the product streams the packed weights once and
  * is bound by HBM); larger n1 gives QZ_ERR_UNSUPPORTED.  mid % 8 == 0, group > 0,
  * mid % group == 0 (QZ_ERR_SHAPE).  Asynchronous on `stream`; needs no workspace. */

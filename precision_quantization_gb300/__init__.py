@@ -39,7 +39,7 @@ BLOCK_SIZE = {QZ_MXFP4: 32, QZ_NVFP4: 16, QZ_INT4: 32}  # INT4: the default grou
 # Names of the exported C symbols (the whole ABI of include/qz.h).
 ABI_SYMBOLS = ("qz_status_string", "qz_workspace_size", "qz_workspace_init", "qz_amax",
                "qz_quantize", "qz_quantize_delayed", "qz_dequantize", "qz_error_stats",
-               "qz_error_stats_noalloc", "qz_stats_merge", "qz_dequantize_asym4", "qz_quant_dot",
+               "qz_error_stats_noalloc", "qz_error_stats_noalloc_status", "qz_stats_merge", "qz_dequantize_asym4", "qz_quant_dot",
                "qz_selftest_pipeline_timeout", "qz_get_device_status")
 
 
@@ -85,6 +85,7 @@ def lib():
             "qz_dequantize": (i32, [dp, vp, vp, vp, vp, i32, vp]),
             "qz_error_stats": (i32, [dp, vp, vp, vp, vp, vp, vp, vp]),
             "qz_error_stats_noalloc": (i32, [dp, vp, vp, vp, vp, vp, vp]),
+            "qz_error_stats_noalloc_status": (i32, [C.POINTER(C.c_uint32), vp]),
             "qz_stats_merge": (i32, [vp, C.c_int64, vp, vp]),
             "qz_get_device_status": (i32, [vp, C.POINTER(C.c_uint32), vp]),
             "qz_dequantize_asym4": (i32, [vp, vp, vp, C.c_int64, C.c_int64, C.c_int64, vp,
@@ -181,6 +182,14 @@ def qz_error_stats_noalloc(desc: QzDesc, x: int, codes: int, scales: int | None,
     uses a fixed scratch array of its own; see include/qz.h)."""
     return lib().qz_error_stats_noalloc(C.byref(desc), x, codes, scales, tensor_scale_dev,
                                         stats_dev, stream)
+
+
+def qz_error_stats_noalloc_status(stream: int = 0) -> tuple[int, int]:
+    """(status, flags): the QZ_FLAG_* bits qz_error_stats_noalloc calls on the current device
+    raised since the last query, read and cleared in order on `stream`."""
+    flags = C.c_uint32(0)
+    st = lib().qz_error_stats_noalloc_status(C.byref(flags), stream)
+    return st, flags.value
 
 
 def qz_stats_merge(parts: int, count: int, out: int, stream: int = 0) -> int:

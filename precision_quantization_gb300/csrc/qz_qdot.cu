@@ -4,11 +4,15 @@
 // 4-bit shift per group of g weights along l, and bf16 activations y.
 //
 // For a few activation columns (n1 <= 8: decoding, small batches) the product streams the
-// packed weights once and does 2 * n1 flops per 4-bit weight, so it runs on the FMA pipe
-// without tensor cores: a warp takes a block of weight rows, its lanes the rows' 32-bit
-// code words (coalesced 128-byte reads), the weights are dequantized in registers exactly
-// as qz_dequantize_asym4 does (fl32(sc * (w - sh))), accumulation is fp32 by paired FMA,
-// and a shuffle reduction across the warp finishes each output.
+// packed weights once and does 2 * n1 flops per 4-bit weight.  Two forms:
+//   - tensor-core form (group % 16 == 0, mid % 64 == 0, 16-byte aligned words): the sum
+//     regrouped as sum over groups of sc * sum (w - sh) y; the inner sums, whose factors
+//     are exact small integers and bf16 values, run on mma.sync (bf16 in, fp32
+//     accumulate), the group scale is one FMA per output and group;
+//   - FMA form (any other group): a warp takes a block of weight rows, its lanes the rows'
+//     32-bit code words (coalesced 128-byte reads), the weights are dequantized in
+//     registers exactly as qz_dequantize_asym4 does (fl32(sc * (w - sh))), accumulation is
+//     fp32 by paired FMA, and a shuffle reduction across the warp finishes each output.
 #include <algorithm>
 
 #include "qz_device.cuh"

@@ -113,3 +113,19 @@ def assert_parity(g, o, stats=True):
     if stats:
         assert_stats_close(g["stats"], o["stats"], "fused")
         assert_stats_close(g["stats2"], o["stats"], "standalone")
+
+
+def qdot_bound(mid: int, group: int) -> int:
+    """E of the quantized-product error bound in include/qz.h: every output is within
+    E * 2^-24 * sum |terms| of the exact sum (tensor-core steps of 16 exact products with
+    truncated alignment, plus one fp32 rounding per weight, group FMA, lane term and split
+    partial)."""
+    def cdiv(a, b):
+        return -(-a // b)
+    return 34 * cdiv(min(group, 1024), 16) + cdiv(mid, 32) + cdiv(mid, 256) + 24
+
+
+def qdot_tolerance(mid: int, group: int, zabs):
+    """Absolute tolerance per output from the oracle's sum of term magnitudes (first-order
+    bound times 1.001 for the second-order terms)."""
+    return qdot_bound(mid, group) * 2.0 ** -24 * 1.001 * zabs + 1e-35

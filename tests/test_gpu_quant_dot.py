@@ -1,12 +1,14 @@
 """GPU parity of the quantized matrix product (qz_quant_dot) against the oracle's exact
-double sum: every output within (2 mid + 8) 2^-24 of the sum of the terms' magnitudes, the
-bound fp32 accumulation in any order guarantees (include/qz.h)."""
+double sum: every output within E 2^-24 of the sum of the terms' magnitudes, with E the
+bound include/qz.h derives from the operations of each form (gpu_util.qdot_bound); and
+bit-exact equality where every partial sum is exact in fp32 (small integer activations,
+power-of-two scales), which a dropped, doubled or misplaced term cannot pass."""
 import numpy as np
 import pytest
 
 import oracle as O
 import workloads as W
-from gpu_util import torch_mod
+from gpu_util import qdot_bound, qdot_tolerance, torch_mod
 
 pytestmark = pytest.mark.gpu
 
@@ -48,8 +50,8 @@ def test_quant_dot_parity(n0, mid, group, n1, ypad, zpad):
                      torch.from_numpy(sh.view(np.int32)).cuda(), group, yd, out=zb[:, :n1])
     torch.cuda.synchronize()
     got = z.cpu().numpy().astype(np.float64)
-    tol = (2 * mid + 8) * 2.0 ** -24 * za + 1e-35
-    assert np.all(np.abs(got - zr) <= tol), float(np.max(np.abs(got - zr) - tol))
+    tol = qdot_tolerance(mid, group, za)
+    assert np.all(np.abs(got - zr) <= tol), float(np.max((np.abs(got - zr) - tol) / za))
     assert np.all(zb[:, n1:].cpu().numpy() == 7.0)  # nothing written past n1
 
 
@@ -64,4 +66,37 @@ def test_quant_dot_weight_like_shape():
                      torch.from_numpy(sh.view(np.int32)).cuda(), 128,
                      torch.from_numpy(y.view(np.int16)).cuda().view(torch.bfloat16))
     got = z.cpu().numpy().astype(np.float64)
-    assert np.all(np.abs(got - zr) <= (2 * mid + 8) * 2.0 ** -24 * za + 1e-35)
+    assert np.all(np.abs(got - zr) <= qdot_tolerance(mid, 128, za))
+
+
+def make_exact(n0, mid, group, n1, seed):
+    """Weights, power-of-two scales (1/4 .. 2), shifts and small-integer activations in
+    [-4, 4]: every term is a multiple of 1/4 below 2^7 and every partial sum a multiple of
+    1/4 below 2^20, all exact in fp32 whatever the order and the accumulator's rounding,
+    so the GPU must give the oracle's sum bit for bit."""
+    rng = np.random.default_rng(seed)
+    ng = mid // group
+    w = pack_words(rng.integers(0, 16, (n0, mid)))
+    sc = (2.0 ** rng.integers(-2, 2, (n0, ng))).astype(np.float32)
+    sh = pack_words(rng.integers(0, 16, (n0, ng)))
+    yi = rng.integers(-4, 5, (mid, n1)).astype(np.float32)
+    y = (yi.view(np.uint32) >> 16).astype(np.uint16)  # exact in bf16
+    return w, sc, sh, np.ascontiguousarray(y)
+
+
+@pytest.mark.parametrize("n0,mid,group,n1", [(129, 8192, 128, 8), (4096, 4096, 64, 8),
+                                             (300, 2048, 16, 4), (33, 1024, 256, 8),
+                                             (9, 520, 40, 7), (64, 96, 12, 1)])
+def test_quant_dot_exact_sums(n0, mid, group, n1):
+    """Tensor-core form (groups of 16 .. 256, split rows) and FMA form (groups of 40, 12):
+    with every partial sum exact the result must equal the oracle's exactly."""
+    import precision_quantization_gb300 as qz
+    torch = torch_mod()
+    w, sc, sh, y = make_exact(n0, mid, group, n1, seed=970 + n0 + group)
+    zr, _ = O.quant_dot(w, sc, sh, y, group)
+    z = qz.quant_dot(torch.from_numpy(w.view(np.int32)).cuda(), torch.from_numpy(sc).cuda(),
+                     torch.from_numpy(sh.view(np.int32)).cuda(), group,
+                     torch.from_numpy(y.view(np.int16)).cuda().view(torch.bfloat16))
+    got = z.cpu().numpy().astype(np.float64)
+    bad = np.argwhere(got != zr)
+    assert bad.size == 0, (len(bad), tuple(bad[0]), got[tuple(bad[0])], zr[tuple(bad[0])])

@@ -657,3 +657,36 @@ def test_quant_dot_integer_and_dyadic_exact(orc):
     deq = sc[:, gi].astype(np.float64) * (codes - shv[:, gi])
     z, _ = orc.quant_dot(w, sc, sh, y, group)
     assert np.array_equal(z, deq @ yi.astype(np.float64))
+
+
+def test_quant_dot_bound_catches_one_dropped_term(orc):
+    """The tolerance the GPU parity tests allow (include/qz.h's E 2^-24 sum|terms|) is
+    smaller than one term of average size at the full-size shapes, so a kernel that drops
+    or doubles a single term fails.  Checked by planting the mistake in the oracle's
+    inputs: zero one weight code's term by setting its code to its group's shift."""
+    from gpu_util import qdot_tolerance
+    rng = np.random.default_rng(46)
+    for n0, mid, group, n1 in ((4, 8192, 128, 8), (4, 4096, 128, 8), (4, 4096, 64, 2)):
+        ng = mid // group
+        codes = rng.integers(0, 16, (n0, mid))
+        shv = rng.integers(0, 16, (n0, ng))
+        sc = (rng.standard_normal((n0, ng)) * 0.02).astype(np.float32)
+
+        def pack(v):
+            out = np.zeros((v.shape[0], (v.shape[1] + 7) // 8), dtype=np.uint32)
+            for i in range(v.shape[1]):
+                out[:, i // 8] |= v[:, i].astype(np.uint32) << np.uint32(4 * (i % 8))
+            return out
+        yf = rng.standard_normal((mid, n1)).astype(np.float32)
+        y = (yf.view(np.uint32) >> 16).astype(np.uint16)
+        z, za = orc.quant_dot(pack(codes), sc, pack(shv), y, group)
+        tol = qdot_tolerance(mid, group, za)
+        # drop, in every row, the term whose magnitude is the row's median (a typical term)
+        c2 = codes.copy()
+        for j in range(n0):
+            gi = np.arange(mid) // group
+            mag = np.abs(sc[j, gi] * (codes[j] - shv[j, gi]) * yf[:, 0].astype(np.float64))
+            l = int(np.argsort(mag)[mid // 2])
+            c2[j, l] = shv[j, l // group]
+        z2, _ = orc.quant_dot(pack(c2), sc, pack(shv), y, group)
+        assert np.all(np.abs(z2[:, 0] - z[:, 0]) > tol[:, 0]), (n0, mid, group)
