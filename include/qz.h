@@ -271,9 +271,9 @@ QZ_API qz_status qz_dequantize_asym4(const uint32_t* w, const float* scales,
  * The sum runs in fp32 in an unspecified order.  With group % 16 == 0 it runs on the tensor
  * cores as sum over groups of sc * sum (w - sh) y: the integer factors w - sh are exact in
  * bf16, every product (w - sh) y is exact in fp32, and the scale is applied by one fp32 FMA
- * per output and group.  Every z[j][k] is within
- *     E * 2^-24 * sum_l |weight * y|,   E = 34 ceil(min(group, 1024) / 16) + ceil(mid / 32)
- *                                            + ceil(mid / 256) + 24
+ * per output and group (and per 1024 values of a longer group).  Every z[j][k] is within
+ *     E * 2^-24 * sum_l |weight * y|,   E = 34 ceil(g' / 16) + ceil(mid / g') + ceil(mid / 32)
+ *                                            + ceil(mid / 256) + 24,   g' = min(group, 1024)
  * of the exact sum.  The 34 per 16 terms covers one tensor-core step c + sum of 16 exact
  * products whose addends are aligned to the largest one and cut to 24 bits (truncation)
  * and whose result is normalised with at most one more ulp: 16 addends lose under one ulp
@@ -281,9 +281,18 @@ QZ_API qz_status qz_dequantize_asym4(const uint32_t* w, const float* scales,
  * other terms count the remaining fp32 roundings of the order used: one per weight
  * rounding, one per group FMA, one per partial sum of split rows (FMA form: one per term a
  * lane accumulates, mid / 32 at most, five in the warp reduction).
- * n1 in [1, 8] (few activation columns: the product streams the packed weights once and
- * is bound by HBM); larger n1 gives QZ_ERR_UNSUPPORTED.  mid % 8 == 0, group > 0,
- * mid % group == 0 (QZ_ERR_SHAPE).  Asynchronous on `stream`; needs no workspace. */
+ * Forms by the number of activation columns:
+ *   n1 <= 8   (decode, small batches): the packed weights are streamed once; the product is
+ *             bound by HBM.  Tensor-core form by mma.sync when group % 16 == 0, mid % 64 == 0
+ *             and w is 16-byte aligned; an FMA form otherwise.
+ *   n1 > 8    (prefill-sized batches): a dense contraction on tcgen05 tensor cores with the
+ *             partial sums in tensor memory, when group % 16 == 0, mid % 64 == 0, w and y
+ *             16-byte aligned and ld_y % 8 == 0; otherwise blocks of 8 columns by the n1 <= 8
+ *             forms (correct, but the weights are read once per block).
+ * mid % 8 == 0, group > 0, mid % group == 0 (QZ_ERR_SHAPE); n1 < 2^30 (QZ_ERR_UNSUPPORTED).
+ * Asynchronous on `stream`; needs no workspace.  A tcgen05 kernel that gives up waiting for
+ * its own copies (never expected: every wait is bounded) writes NaN to the outputs of its
+ * tiles instead of hanging. */
 QZ_API qz_status qz_quant_dot(const uint32_t* w, const float* scales, const uint32_t* shifts,
                               int64_t n0, int64_t mid, int64_t group, const void* y, int64_t ld_y,
                               int64_t n1, float* z, int64_t ld_z, qz_stream_t stream);

@@ -146,7 +146,8 @@ def qz_quant_dot(w: int, scales: int, shifts: int, n0: int, mid: int, group: int
 def quant_dot(w, scales, shifts, group: int, y, out=None, stream=None):
     """z = sum_l sc (w - sh) y (see qz_quant_dot): w int32/uint32 CUDA tensor [n0, mid/8],
     scales fp32 [n0, mid/group], shifts int32/uint32 [n0, ceil(mid/group/8)], y bf16
-    [mid, n1] (n1 <= 8).  Returns fp32 [n0, n1]."""
+    [mid, n1] (any n1: up to 8 columns stream the weights once, more run on the tcgen05
+    tensor cores).  Returns fp32 [n0, n1]."""
     torch = _torch()
     n0, wpr = w.shape
     mid, n1 = y.shape

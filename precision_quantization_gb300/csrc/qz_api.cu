@@ -381,7 +381,7 @@ extern "C" qz_status qz_quant_dot(const uint32_t* w, const float* scales, const 
   if (n0 < 0 || mid < 0 || n1 < 0 || group <= 0 || mid % 8 != 0 || mid % group != 0 || ld_y < n1 ||
       ld_z < n1)
     return QZ_ERR_SHAPE;
-  if (n1 > 8) return QZ_ERR_UNSUPPORTED;
+  if (n1 >= (int64_t{1} << 30) || n0 >= (int64_t{1} << 40)) return QZ_ERR_UNSUPPORTED;
   if ((mid > 0 && ld_y > 0 && mid > (INT64_MAX / 8) / ld_y) || (n0 > 0 && ld_z > 0 && n0 > (INT64_MAX / 8) / ld_z))
     return QZ_ERR_SHAPE;
   if (n0 * n1 == 0) return QZ_OK;

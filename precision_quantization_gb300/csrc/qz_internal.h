@@ -66,6 +66,13 @@ qz_status launch_dequant_asym4(const uint32_t* w, const float* scales, const uin
                                int out_dtype, cudaStream_t s);
 // z[j][0 .. n1) = 0 for j < n0 (rows ld_z floats apart)
 qz_status launch_zero_z(float* z, int64_t ld_z, int64_t n0, int64_t n1, cudaStream_t s);
+// the tensor-core (tcgen05) product for many activation columns: applicable when n1 > 8,
+// group % 16 == 0, mid % 64 == 0, w and y 16-byte aligned and ld_y % 8 == 0
+bool quant_dot_tc_applicable(const uint32_t* w, int64_t n0, int64_t mid, int64_t group, const void* y,
+                             int64_t ld_y, int64_t n1);
+qz_status launch_quant_dot_tc(const uint32_t* w, const float* scales, const uint32_t* shifts, int64_t n0,
+                              int64_t mid, int64_t group, const void* y, int64_t ld_y, int64_t n1, float* z,
+                              int64_t ld_z, cudaStream_t s);
 qz_status launch_quant_dot(const uint32_t* w, const float* scales, const uint32_t* shifts,
                            int64_t n0, int64_t mid, int64_t group, const void* y, int64_t ld_y,
                            int64_t n1, float* z, int64_t ld_z, cudaStream_t s);

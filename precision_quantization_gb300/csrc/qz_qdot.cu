@@ -514,19 +514,10 @@ qz_status run(QdArgs a, bool yvec, cudaStream_t s) {
   return launch_status();
 }
 
-}  // namespace
-
-qz_status launch_zero_z(float* z, int64_t ld_z, int64_t n0, int64_t n1, cudaStream_t s) {
-  const int64_t n = n0 * n1;
-  if (n == 0) return QZ_OK;
-  const int64_t ctas = std::min<int64_t>((n + kThreads - 1) / kThreads, static_cast<int64_t>(sm_count()) * 8);
-  zero_z_kernel<<<static_cast<int>(ctas), kThreads, 0, s>>>(z, ld_z, n0, static_cast<int>(n1));
-  return launch_status();
-}
-
-qz_status launch_quant_dot(const uint32_t* w, const float* scales, const uint32_t* shifts,
-                           int64_t n0, int64_t mid, int64_t group, const void* y, int64_t ld_y,
-                           int64_t n1, float* z, int64_t ld_z, cudaStream_t s) {
+// n1 <= 8 columns: the tensor-core (mma.sync) form or the FMA form
+qz_status quant_dot_few(const uint32_t* w, const float* scales, const uint32_t* shifts, int64_t n0, int64_t mid,
+                        int64_t group, const void* y, int64_t ld_y, int64_t n1, float* z, int64_t ld_z,
+                        cudaStream_t s) {
   const QdArgs a{w, scales, shifts, static_cast<const uint16_t*>(y), z, n0, mid, group, ld_y, ld_z, 1, 0};
   const bool yvec = reinterpret_cast<uintptr_t>(y) % 16 == 0 && ld_y % 8 == 0;
   qz_status st = QZ_OK;
@@ -543,6 +534,32 @@ qz_status launch_quant_dot(const uint32_t* w, const float* scales, const uint32_
     case 7: return run<7>(a, yvec, s);
     default: return run<8>(a, yvec, s);
   }
+}
+
+}  // namespace
+
+qz_status launch_zero_z(float* z, int64_t ld_z, int64_t n0, int64_t n1, cudaStream_t s) {
+  const int64_t n = n0 * n1;
+  if (n == 0) return QZ_OK;
+  const int64_t ctas = std::min<int64_t>((n + kThreads - 1) / kThreads, static_cast<int64_t>(sm_count()) * 8);
+  zero_z_kernel<<<static_cast<int>(ctas), kThreads, 0, s>>>(z, ld_z, n0, static_cast<int>(n1));
+  return launch_status();
+}
+
+qz_status launch_quant_dot(const uint32_t* w, const float* scales, const uint32_t* shifts,
+                           int64_t n0, int64_t mid, int64_t group, const void* y, int64_t ld_y,
+                           int64_t n1, float* z, int64_t ld_z, cudaStream_t s) {
+  if (n1 <= 8) return quant_dot_few(w, scales, shifts, n0, mid, group, y, ld_y, n1, z, ld_z, s);
+  if (quant_dot_tc_applicable(w, n0, mid, group, y, ld_y, n1))
+    return launch_quant_dot_tc(w, scales, shifts, n0, mid, group, y, ld_y, n1, z, ld_z, s);
+  // shapes the tensor-memory kernel does not take (groups that are not a multiple of 16,
+  // unaligned activations): blocks of 8 columns, each streaming the weights once more
+  for (int64_t k = 0; k < n1; k += 8) {
+    const qz_status st = quant_dot_few(w, scales, shifts, n0, mid, group, static_cast<const uint16_t*>(y) + k,
+                                       ld_y, std::min<int64_t>(8, n1 - k), z + k, ld_z, s);
+    if (st != QZ_OK) return st;
+  }
+  return QZ_OK;
 }
 
 }  // namespace qz

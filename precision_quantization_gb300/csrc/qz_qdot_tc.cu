@@ -1,0 +1,570 @@
+// qz_qdot_tc.cu -- the quantized matrix product of the blog's "Puzzles 12 Quantized Matrix
+// Mult" (section of its "Triton" post) for many activation columns, on the sm_103a tensor
+// cores (tcgen05.mma, accumulators in tensor memory):
+//     z[j][k] = sum_l sc[j][l/g] (w[j][l] - sh[j][l/g]) y[l][k]
+// with 4-bit weights w (8 per 32-bit word, low nibble first), one fp32 scale and one 4-bit
+// shift per group of g weights along l, and bf16 activations y [mid, n1].
+//
+// With many columns (prefill-sized batches) the product does 2 n1 flops per weight and is
+// a dense contraction.  The sum is regrouped as sum over groups of sc * P_g with
+// P_g = sum_{l in g} (w - sh) y: w - sh is an integer in [-15, 15], exact in bf16, and every
+// product with a bf16 y is exact in fp32, so P_g runs on the tensor cores (kind::f16, bf16
+// operands, fp32 accumulation) and the scale is applied by one fp32 FMA per output and
+// group, keeping the result within the bound include/qz.h states.
+//
+// One CTA per SM, persistent over work items (a tile of 128 weight rows x up to 256
+// activation columns, times one slice of l when the tiles are too few to fill the GPU).
+// Roles (warp-specialised, every wait bounded in time):
+//   warp 0        lane 0 streams each 64-wide l-step into a ring of kStages shared-memory
+//                 stages by TMA: the tile's 128 x 8 code words and up to four 64 x 64 bf16
+//                 boxes of y (128-byte swizzle, activation columns contiguous: the MMA's
+//                 "MN-major" B operand).  The warp also owns the tensor-memory allocation.
+//   warp 1        lane 0 issues the MMAs: four 128 x N x 16 steps per stage into one of two
+//                 tensor-memory buffers of 256 fp32 columns, a new buffer at every group
+//                 boundary (and every 1024 values of a longer group), commits each stage's
+//                 completion to its "empty" barrier and each finished group to "P full".
+//   warps 2-3     decode: each thread takes two weight rows of the stage, turns every code
+//                 word into eight bf16 values w - sh (nibbles split by mask, paired by a
+//                 byte permute, OR-ed into bf16 128 + w, one bf16x2 add of -(128 + sh)) and
+//                 stores them in the MMA's K-major 128-byte swizzled layout, then signals
+//                 "A full".
+//   warps 4-19    epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. + 31 (its rows)
+//                 and 64 of the 256 columns; for every finished group it adds sc * P into
+//                 64 fp32 registers, frees the buffer, and at the end of the item stores z
+//                 (atomic adds when the item is one slice of several).
+#include <cuda.h>  // CUtensorMap and its enumerators (types only; the encoder is looked up)
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "qz_device.cuh"
+#include "qz_internal.h"
+#include "qz_pipe.cuh"
+
+namespace qz {
+namespace {
+
+constexpr int kBM = 128;        // weight rows per tile (MMA M, tensor-memory lanes)
+constexpr int kBN = 256;        // activation columns per tile (MMA N at most)
+constexpr int kBK = 64;         // l per stage (one 128-byte swizzle row of bf16)
+constexpr int kStages = 4;
+constexpr int kDecWarps = 2;
+constexpr int kEpiWarps = 16;
+constexpr int kFirstDec = 2, kFirstEpi = kFirstDec + kDecWarps;
+constexpr int kWarpsTc = kFirstEpi + kEpiWarps;  // 20
+constexpr int kThreadsTc = 32 * kWarpsTc;        // 640
+constexpr uint32_t kSlabBytes = 64 * kBK * 2;    // one 64-column box of y: 8 KiB
+constexpr uint32_t kBBytes = 4 * kSlabBytes;     // 32 KiB
+constexpr uint32_t kABytes = kBM * kBK * 2;      // 16 KiB of decoded bf16 weights
+constexpr uint32_t kRawBytes = kBM * kBK / 2;    // 4 KiB of code words
+constexpr uint32_t kStageBytes = kBBytes + kABytes + kRawBytes;  // 52 KiB, a multiple of 1 KiB
+constexpr uint32_t kSmemTc = kStages * kStageBytes + 1024;       // + alignment slack
+constexpr int kPieceCap = 1024;  // values of one group accumulated per tensor-memory buffer
+constexpr uint32_t kTmemCols = 512;  // two buffers of 256 fp32 columns
+constexpr uint64_t kTcWaitNs = 1000000000ull;  // 1 s: far beyond any step's latency
+
+struct TcParams {
+  CUtensorMap tmap_y;  // bf16 y [mid rows][n1 columns], box 64 x 64, 128-byte swizzle
+  CUtensorMap tmap_w;  // uint32 w [n0 rows][mid / 8 words], box 8 x 128
+  const float* scales;
+  const uint32_t* shifts;
+  float* z;
+  int64_t ld_z;
+  int n0, n1, mid, group, ng, sw;
+  int tiles_n, ksplit, slice_stages, stages_total, items;
+};
+
+// ---- small PTX wrappers -----------------------------------------------------------------
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem] for one 128 x N x 16 step
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, bool acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc ? 1u : 0u)
+      : "memory");
+}
+// 16 consecutive fp32 columns of this thread's tensor-memory lane
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+__device__ __forceinline__ uint4 lds128_tc(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+  return v;
+}
+
+// Shared-memory matrix descriptor of tcgen05 (start address, leading and stride byte
+// offsets in 16-byte units, descriptor version 1, 128-byte swizzle).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(lbo >> 4) << 16) |
+         (static_cast<uint64_t>(sbo >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, A K-major, B MN-major,
+// N = n columns, M = 128.
+__device__ __forceinline__ uint32_t idesc_bf16(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(kBM >> 4) << 24);
+}
+
+// Bounded wait on phase `parity` of a barrier; gives up (and raises the CTA's abort flag)
+// after kTcWaitNs, or at once when another role has given up already.
+__device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kTcWaitNs) {
+      *abort = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
+// The work item's tile and l range.
+struct Item {
+  int m0, nb, st0, nst;  // first weight row, first column, first stage, stages
+  int nslab;             // 64-column boxes of y that hold columns < n1 (1 .. 4)
+};
+__device__ __forceinline__ Item item_of(const TcParams& p, int it) {
+  Item r;
+  const int s = it % p.ksplit, t = it / p.ksplit;
+  r.m0 = (t / p.tiles_n) * kBM;
+  r.nb = (t % p.tiles_n) * kBN;
+  r.st0 = s * p.slice_stages;
+  r.nst = min(p.slice_stages, p.stages_total - r.st0);
+  r.nslab = min(4, (p.n1 - r.nb + 63) / 64);
+  return r;
+}
+// does a new accumulation piece start at l (a multiple of 16, inside the item's range)?
+__device__ __forceinline__ bool piece_start(int l, int l_begin, int group) {
+  return l == l_begin || l % group == 0 || (group > kPieceCap && l % kPieceCap == 0);
+}
+
+__global__ void __launch_bounds__(kThreadsTc, 1) quant_dot_tc_kernel(const __grid_constant__ TcParams p) {
+  extern __shared__ uint8_t tc_smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[kStages], afull_bar[kStages], empty_bar[kStages];
+  __shared__ __align__(8) uint64_t pfull_bar[2], pempty_bar[2], drain_bar;
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t base = (smem_addr(tc_smem_raw) + 1023u) & ~1023u;  // 1 KiB-aligned stages
+  const auto b_of = [&](int s) { return base + static_cast<uint32_t>(s) * kStageBytes; };
+  const auto a_of = [&](int s) { return b_of(s) + kBBytes; };
+  const auto raw_of = [&](int s) { return b_of(s) + kBBytes + kABytes; };
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_addr(&full_bar[s]), 1);
+      mbar_init(smem_addr(&afull_bar[s]), kDecWarps);
+      mbar_init(smem_addr(&empty_bar[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_addr(&pfull_bar[b]), 1);
+      mbar_init(smem_addr(&pempty_bar[b]), kEpiWarps);
+    }
+    mbar_init(smem_addr(&drain_bar), 1);
+    mbar_init_fence();
+    s_abort = 0;
+  }
+  if (warp == 0) {  // the whole warp allocates the two accumulator buffers
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const int first_item = blockIdx.x, item_step = gridDim.x;
+
+  if (warp == 0) {
+    // ---------------- TMA producer (the whole warp waits; lane 0 issues) ----------------
+    int stage = 0;
+    uint32_t phase = 0;
+    int inflight = 0;  // stages issued and not yet known to have landed (for the drain)
+    for (int it = first_item; it < p.items && !s_abort; it += item_step) {
+      const Item I = item_of(p, it);
+      for (int st = 0; st < I.nst; ++st) {
+        if (!__all_sync(kFull, tc_wait(smem_addr(&empty_bar[stage]), phase ^ 1u, &s_abort))) break;
+        if (lane == 0) {
+          const uint32_t fb = smem_addr(&full_bar[stage]);
+          const int l0 = (I.st0 + st) * kBK;
+          mbar_expect_tx(fb, kRawBytes + kSlabBytes * static_cast<uint32_t>(I.nslab));
+          tma_load_2d(raw_of(stage), &p.tmap_w, l0 / 8, I.m0, fb);
+          for (int sl = 0; sl < I.nslab; ++sl)
+            tma_load_2d(b_of(stage) + sl * kSlabBytes, &p.tmap_y, I.nb + 64 * sl, l0, fb);
+        }
+        __syncwarp();
+        inflight = min(inflight + 1, kStages);
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (s_abort && lane == 0) {
+      // let the copies already issued land before the shared memory is released: the
+      // last `inflight` stages before `stage` (bounded waits; a timeout just ends it)
+      for (int k = 1; k <= inflight; ++k) {
+        const int s = (stage - k + kStages) % kStages;
+        const uint32_t ph = (stage - k < 0) ? (phase ^ 1u) : phase;
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(smem_addr(&full_bar[s]), ph) && globaltimer_ns() - t0 < kTcWaitNs) {
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (the whole warp waits; lane 0 issues) ----------------
+    int stage = 0, buf = 0;
+    uint32_t phase = 0, pe_bits = 3u;  // bit b: parity of the next wait on "P empty" b
+    bool issued = false;
+    for (int it = first_item; it < p.items && !s_abort; it += item_step) {
+      const Item I = item_of(p, it);
+      const uint32_t idesc = idesc_bf16(64 * I.nslab);
+      const int l_begin = I.st0 * kBK;
+      bool open = false, acc = false;
+      for (int st = 0; st < I.nst; ++st) {
+        if (!__all_sync(kFull, tc_wait(smem_addr(&full_bar[stage]), phase, &s_abort))) break;
+        if (!__all_sync(kFull, tc_wait(smem_addr(&afull_bar[stage]), phase, &s_abort))) break;
+        tc_fence_after();
+        const int l0 = (I.st0 + st) * kBK;
+        bool ok = true;
+#pragma unroll
+        for (int j = 0; j < kBK / 16; ++j) {
+          const int l = l0 + 16 * j;
+          if (piece_start(l, l_begin, p.group)) {
+            if (open) {
+              if (lane == 0) tc_commit(smem_addr(&pfull_bar[buf]));
+              __syncwarp();
+              buf ^= 1;
+            }
+            if (!__all_sync(kFull, tc_wait(smem_addr(&pempty_bar[buf]), (pe_bits >> buf) & 1u, &s_abort))) {
+              ok = false;
+              break;
+            }
+            pe_bits ^= 1u << buf;
+            tc_fence_after();
+            open = true;
+            acc = false;
+          }
+          // A: rows of 128 bytes, 8-row groups 1 KiB apart, +32 bytes per 16 values of l;
+          // B: 64-column boxes 8 KiB apart, 8-row groups of l 1 KiB apart, +2 KiB per 16 l
+          if (lane == 0) {
+            const uint64_t ad = smem_desc_sw128(a_of(stage) + 32u * j, 16u, 1024u);
+            const uint64_t bd = smem_desc_sw128(b_of(stage) + 2048u * j, kSlabBytes, 1024u);
+            tc_mma(tmem + static_cast<uint32_t>(buf) * kBN, ad, bd, idesc, acc);
+          }
+          __syncwarp();
+          acc = true;
+          issued = true;
+        }
+        if (!ok) break;
+        if (lane == 0) tc_commit(smem_addr(&empty_bar[stage]));
+        __syncwarp();
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (s_abort) break;
+      if (open) {
+        if (lane == 0) tc_commit(smem_addr(&pfull_bar[buf]));
+        __syncwarp();
+        buf ^= 1;
+      }
+    }
+    if (issued && lane == 0) {  // every MMA issued has completed before tensor memory is released
+      tc_commit(smem_addr(&drain_bar));
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(smem_addr(&drain_bar), 0u) && globaltimer_ns() - t0 < kTcWaitNs) {
+      }
+    }
+    __syncwarp();
+  } else if (warp < kFirstEpi) {
+    // ---------------- decoders: code words -> bf16 (w - sh), swizzled K-major ----------------
+    // Each thread keeps, for each of its two rows, the shift word of its current group and
+    // the one after it in registers: the next word is loaded as soon as the current one is
+    // taken, at least eight groups before it is needed, so no global load latency sits
+    // on the path of a stage.
+    const int dt = tid - 32 * kFirstDec;  // 0 .. 63: rows dt and dt + 64 of the tile
+    int stage = 0;
+    uint32_t phase = 0;
+    const int wpg = p.group / 8;  // code words per group (group % 16 == 0)
+    for (int it = first_item; it < p.items && !s_abort; it += item_step) {
+      const Item I = item_of(p, it);
+      int widx[2];
+      uint32_t wcur[2], wnxt[2];
+      const int gfirst = I.st0 * (kBK / 8) / wpg;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int row = I.m0 + dt + 64 * h;
+        const uint32_t* sr = p.shifts + static_cast<int64_t>(row < p.n0 ? row : 0) * p.sw;
+        widx[h] = gfirst >> 3;
+        wcur[h] = row < p.n0 ? __ldg(sr + widx[h]) : 0u;
+        wnxt[h] = (row < p.n0 && widx[h] + 1 < p.sw) ? __ldg(sr + widx[h] + 1) : 0u;
+      }
+      for (int st = 0; st < I.nst; ++st) {
+        if (!__all_sync(kFull, tc_wait(smem_addr(&full_bar[stage]), phase, &s_abort))) break;
+        const int w0 = (I.st0 + st) * (kBK / 8);  // first code word of the stage in the row
+        const int g0 = w0 / wpg, left0 = (g0 + 1) * wpg - w0;  // its group, words left in it
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int r = dt + 64 * h;
+          const int row = I.m0 + r;
+          const uint4 c0 = lds128_tc(raw_of(stage) + 32u * r);
+          const uint4 c1 = lds128_tc(raw_of(stage) + 32u * r + 16u);
+          const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          const uint32_t arow = a_of(stage) + 128u * r;
+          int g = g0, left = left0;  // group of word c, and its words still to come
+          uint32_t addc = 0u;        // bf16 pair (-(128 + sh), -(128 + sh)) of group g
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            if (c == 0 || left == 0) {
+              if (c != 0) {
+                ++g;
+                left = wpg;
+              }
+              if ((g >> 3) != widx[h]) {  // groups advance one at a time: the next word
+                widx[h] = g >> 3;
+                wcur[h] = wnxt[h];
+                wnxt[h] = (row < p.n0 && widx[h] + 1 < p.sw)
+                              ? __ldg(p.shifts + static_cast<int64_t>(row) * p.sw + widx[h] + 1)
+                              : 0u;
+              }
+              const uint32_t sh = (wcur[h] >> (4 * (g & 7))) & 0xFu;
+              addc = 0xC300C300u + 0x00010001u * sh;  // bf16 -(128 + sh): ulp 1 at 128
+            }
+            --left;
+            // even nibbles (elements 0, 2, 4, 6) in bytes 0..3 of t0, odd ones in t1; value
+            // pair q is bytes q of t0 and t1 side by side, OR 0x4300 in each half is the
+            // bf16 128 + nibble, and one bf16x2 add of -(128 + sh) leaves w - sh exactly
+            const uint32_t t0 = cw[c] & 0x0F0F0F0Fu, t1 = (cw[c] >> 4) & 0x0F0F0F0Fu;
+            uint32_t v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t d, x;
+              asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(t0), "r"(t1), "r"(0x0400u * 0x11u + q * 0x0101u));
+              asm("lop3.b32 %0, %1, 0x000F000F, 0x43004300, 0xEA;" : "=r"(x) : "r"(d));  // (a & b) | c
+              asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(v[q]) : "r"(x), "r"(addc));
+            }
+            sts128(arow + static_cast<uint32_t>(((c ^ (r & 7)) << 4)), v[0], v[1], v[2], v[3]);
+          }
+        }
+        fence_proxy_async();  // generic-proxy stores -> visible to the tensor cores
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&afull_bar[stage]));
+        if (++stage == kStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+  } else {
+    // ---------------- epilogue ----------------
+    const int q = warp & 3;                 // tensor-memory lane quarter of this warp
+    const int cq = (warp - kFirstEpi) >> 2; // its 64-column quarter of the tile
+    const int r = 32 * q + lane;            // tile row of this thread
+    uint32_t pf_bits = 0u;  // bit b: parity of the next wait on "P full" b
+    // rows of z 16-byte aligned: vector stores
+    const bool zvec = (reinterpret_cast<uintptr_t>(p.z) & 15u) == 0 && (p.ld_z & 3) == 0;
+    int buf = 0;
+    for (int it = first_item; it < p.items && !s_abort; it += item_step) {
+      const Item I = item_of(p, it);
+      const int row = I.m0 + r;
+      const bool row_ok = row < p.n0;
+      float z[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) z[i] = 0.0f;
+      const int l_begin = I.st0 * kBK, l_end = l_begin + I.nst * kBK;
+      bool ok = true;
+      for (int l = l_begin; l < l_end;) {
+        int nxt = min(l_end, (l / p.group + 1) * p.group);
+        if (p.group > kPieceCap) nxt = min(nxt, (l / kPieceCap + 1) * kPieceCap);
+        const int g = l / p.group;
+        const float sc = row_ok ? __ldg(p.scales + static_cast<int64_t>(row) * p.ng + g) : 0.0f;
+        if (!__all_sync(kFull, tc_wait(smem_addr(&pfull_bar[buf]), (pf_bits >> buf) & 1u, &s_abort))) {
+          ok = false;
+          break;
+        }
+        pf_bits ^= 1u << buf;
+        tc_fence_after();
+        const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(buf * kBN + 64 * cq);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float v[16];
+          tmem_ld16(ta + 16u * c, v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) z[16 * c + i] = __fmaf_rn(sc, v[i], z[16 * c + i]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&pempty_bar[buf]));
+        buf ^= 1;
+        l = nxt;
+      }
+      if (!ok) break;
+      if (row_ok) {
+        const int c0 = I.nb + 64 * cq;
+        float* zr = p.z + static_cast<int64_t>(row) * p.ld_z + c0;
+        const int nv = min(64, p.n1 - c0);
+        if (nv == 64 && zvec) {  // 16-byte stores (or reductions): 64 contiguous bytes a pair
+#pragma unroll
+          for (int i = 0; i < 64; i += 4) {
+            if (p.ksplit > 1)
+              asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(zr + i), "f"(z[i]),
+                           "f"(z[i + 1]), "f"(z[i + 2]), "f"(z[i + 3])
+                           : "memory");
+            else
+              asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(zr + i), "f"(z[i]), "f"(z[i + 1]),
+                           "f"(z[i + 2]), "f"(z[i + 3])
+                           : "memory");
+          }
+        } else if (p.ksplit > 1) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (i < nv) atomicAdd(zr + i, z[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (i < nv) zr[i] = z[i];
+        }
+      }
+    }
+  }
+
+  // every role is done (or has given up) and every MMA has completed: release the
+  // tensor memory, and report a give-up as NaN in this CTA's outputs
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+  if (s_abort && warp >= kFirstEpi) {
+    const int q = warp & 3, cq = (warp - kFirstEpi) >> 2, r = 32 * q + lane;
+    for (int it = first_item; it < p.items; it += item_step) {
+      const Item I = item_of(p, it);
+      const int row = I.m0 + r, c0 = I.nb + 64 * cq;
+      if (row >= p.n0) continue;
+      for (int i = 0; i < 64 && c0 + i < p.n1; ++i)
+        p.z[static_cast<int64_t>(row) * p.ld_z + c0 + i] = __uint_as_float(0x7fc00000u);
+    }
+  }
+}
+
+// ---- host side ----------------------------------------------------------------------------
+std::mutex g_encode_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::lock_guard<std::mutex> lock(g_encode_mu);
+  if (!g_encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return g_encode;
+}
+
+}  // namespace
+
+bool quant_dot_tc_applicable(const uint32_t* w, int64_t n0, int64_t mid, int64_t group, const void* y,
+                             int64_t ld_y, int64_t n1) {
+  return n1 > 8 && group % 16 == 0 && mid % kBK == 0 && mid < (int64_t{1} << 30) && n0 < (int64_t{1} << 30) &&
+         n1 < (int64_t{1} << 30) && ld_y % 8 == 0 && reinterpret_cast<uintptr_t>(y) % 16 == 0 &&
+         reinterpret_cast<uintptr_t>(w) % 16 == 0;
+}
+
+qz_status launch_quant_dot_tc(const uint32_t* w, const float* scales, const uint32_t* shifts, int64_t n0,
+                              int64_t mid, int64_t group, const void* y, int64_t ld_y, int64_t n1, float* z,
+                              int64_t ld_z, cudaStream_t s) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  if (!enc) return QZ_ERR_CUDA;
+  TcParams p{};
+  {  // y: dimension 0 = columns (contiguous), dimension 1 = l
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(n1), static_cast<cuuint64_t>(mid)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld_y) * 2};
+    const cuuint32_t box[2] = {64, kBK}, es[2] = {1, 1};
+    if (enc(&p.tmap_y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(y), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return QZ_ERR_CUDA;
+  }
+  {  // w: dimension 0 = code words of a row, dimension 1 = rows
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(mid / 8), static_cast<cuuint64_t>(n0)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(mid / 8) * 4};
+    const cuuint32_t box[2] = {kBK / 8, kBM}, es[2] = {1, 1};
+    if (enc(&p.tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(w), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return QZ_ERR_CUDA;
+  }
+  const int sms = sm_count();
+  const int64_t tiles_m = (n0 + kBM - 1) / kBM, tiles_n = (n1 + kBN - 1) / kBN;
+  const int64_t tiles = tiles_m * tiles_n, stages_total = mid / kBK;
+  // split l when the tiles alone leave SMs idle, keeping slices of at least 256 values
+  int64_t ksplit = 1;
+  if (tiles < sms) ksplit = std::max<int64_t>(1, std::min<int64_t>((sms + tiles - 1) / tiles, stages_total / 4));
+  const int64_t slice_stages = (stages_total + ksplit - 1) / ksplit;
+  ksplit = (stages_total + slice_stages - 1) / slice_stages;
+  const int64_t items = tiles * ksplit;
+  if (items >= (int64_t{1} << 31)) return QZ_ERR_UNSUPPORTED;
+  p.scales = scales;
+  p.shifts = shifts;
+  p.z = z;
+  p.ld_z = ld_z;
+  p.n0 = static_cast<int>(n0);
+  p.n1 = static_cast<int>(n1);
+  p.mid = static_cast<int>(mid);
+  p.group = static_cast<int>(group);
+  p.ng = static_cast<int>(mid / group);
+  p.sw = static_cast<int>((mid / group + 7) / 8);
+  p.tiles_n = static_cast<int>(tiles_n);
+  p.ksplit = static_cast<int>(ksplit);
+  p.slice_stages = static_cast<int>(slice_stages);
+  p.stages_total = static_cast<int>(stages_total);
+  p.items = static_cast<int>(items);
+  if (!set_dyn_smem(reinterpret_cast<const void*>(&quant_dot_tc_kernel), static_cast<int>(kSmemTc)))
+    return QZ_ERR_CUDA;
+  if (ksplit > 1 && launch_zero_z(z, ld_z, n0, n1, s) != QZ_OK) return QZ_ERR_CUDA;
+  const int grid = static_cast<int>(std::min<int64_t>(items, sms));
+  quant_dot_tc_kernel<<<grid, kThreadsTc, kSmemTc, s>>>(p);
+  return launch_status();
+}
+
+}  // namespace qz

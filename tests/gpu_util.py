@@ -118,11 +118,12 @@ def assert_parity(g, o, stats=True):
 def qdot_bound(mid: int, group: int) -> int:
     """E of the quantized-product error bound in include/qz.h: every output is within
     E * 2^-24 * sum |terms| of the exact sum (tensor-core steps of 16 exact products with
-    truncated alignment, plus one fp32 rounding per weight, group FMA, lane term and split
-    partial)."""
+    truncated alignment, plus one fp32 rounding per weight, group piece FMA, lane term and
+    split partial)."""
     def cdiv(a, b):
         return -(-a // b)
-    return 34 * cdiv(min(group, 1024), 16) + cdiv(mid, 32) + cdiv(mid, 256) + 24
+    g = min(group, 1024)
+    return 34 * cdiv(g, 16) + cdiv(mid, g) + cdiv(mid, 32) + cdiv(mid, 256) + 24
 
 
 def qdot_tolerance(mid: int, group: int, zabs):

@@ -170,7 +170,10 @@ def test_asym4_argument_errors_host(qz):
 def test_quant_dot_argument_errors_host(qz):
     F = FAKE
     qd = qz.qz_quant_dot
-    assert qd(F, F, F, 4, 64, 16, F, 9, 9, F, 9) == qz.QZ_ERR_UNSUPPORTED       # n1 > 8
+    big = 1 << 30
+    assert qd(F, F, F, 4, 64, 16, F, big, big, F, big) == qz.QZ_ERR_UNSUPPORTED  # n1 >= 2^30
+    assert qd(None, F, F, 4, 64, 16, F, 300, 300, F, 300) == qz.QZ_ERR_NULL     # many columns
+    assert qd(F, F, F, 4, 64, 16, F + 1, 300, 300, F, 300) == qz.QZ_ERR_ALIGN
     assert qd(F, F, F, 4, 60, 4, F, 8, 8, F, 8) == qz.QZ_ERR_SHAPE              # mid % 8
     assert qd(F, F, F, 4, 64, 24, F, 8, 8, F, 8) == qz.QZ_ERR_SHAPE             # mid % group
     assert qd(F, F, F, 4, 64, 16, F, 4, 8, F, 8) == qz.QZ_ERR_SHAPE             # ld_y < n1

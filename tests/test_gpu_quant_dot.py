@@ -100,3 +100,73 @@ def test_quant_dot_exact_sums(n0, mid, group, n1):
     got = z.cpu().numpy().astype(np.float64)
     bad = np.argwhere(got != zr)
     assert bad.size == 0, (len(bad), tuple(bad[0]), got[tuple(bad[0])], zr[tuple(bad[0])])
+
+
+# ---- many activation columns: the tcgen05 tensor-memory product -------------------------
+@pytest.mark.parametrize("ypad,zpad", [(0, 0), (8, 3), (5, 0)])
+@pytest.mark.parametrize("n0,mid,group,n1", [(300, 1024, 128, 300), (128, 2048, 64, 256),
+                                             (200, 4096, 16, 72), (64, 960, 48, 40),
+                                             (130, 4096, 2048, 24), (257, 512, 256, 9),
+                                             (40, 640, 32, 520)])
+def test_quant_dot_many_columns_parity(n0, mid, group, n1, ypad, zpad):
+    """Ragged tiles in both dimensions, groups that end inside a 64-wide step (16, 32, 48),
+    groups longer than one accumulation piece (2048), split sums (few row tiles), padded
+    rows of y and z, and an unaligned y row pitch (ypad 5: the column-block path)."""
+    import precision_quantization_gb300 as qz
+    torch = torch_mod()
+    w, sc, sh, y = make(n0, mid, group, n1, seed=990 + n0 + n1)
+    zr, za = O.quant_dot(w, sc, sh, y, group)
+    yb = torch.zeros((mid, n1 + ypad), dtype=torch.int16, device="cuda")
+    yb[:, :n1] = torch.from_numpy(y.view(np.int16)).cuda()
+    yd = yb.view(torch.bfloat16)[:, :n1]
+    zb = torch.full((n0, n1 + zpad), 7.0, dtype=torch.float32, device="cuda")
+    z = qz.quant_dot(torch.from_numpy(w.view(np.int32)).cuda(), torch.from_numpy(sc).cuda(),
+                     torch.from_numpy(sh.view(np.int32)).cuda(), group, yd, out=zb[:, :n1])
+    torch.cuda.synchronize()
+    got = z.cpu().numpy().astype(np.float64)
+    tol = qdot_tolerance(mid, group, za)
+    assert np.all(np.abs(got - zr) <= tol), float(np.max((np.abs(got - zr) - tol) / za))
+    assert np.all(zb[:, n1:].cpu().numpy() == 7.0)  # nothing written past n1
+
+
+@pytest.mark.parametrize("n0,mid,group,n1", [(129, 8192, 128, 64), (300, 2048, 32, 300),
+                                             (128, 1024, 1024, 256), (77, 4096, 2048, 33)])
+def test_quant_dot_many_columns_exact_sums(n0, mid, group, n1):
+    """Every partial sum exact in fp32: the tensor-memory product must equal the oracle bit
+    for bit, whatever the accumulation order, so no term may be dropped, doubled or moved."""
+    import precision_quantization_gb300 as qz
+    torch = torch_mod()
+    w, sc, sh, y = make_exact(n0, mid, group, n1, seed=1010 + n0 + group)
+    zr, _ = O.quant_dot(w, sc, sh, y, group)
+    z = qz.quant_dot(torch.from_numpy(w.view(np.int32)).cuda(), torch.from_numpy(sc).cuda(),
+                     torch.from_numpy(sh.view(np.int32)).cuda(), group,
+                     torch.from_numpy(y.view(np.int16)).cuda().view(torch.bfloat16))
+    got = z.cpu().numpy().astype(np.float64)
+    bad = np.argwhere(got != zr)
+    assert bad.size == 0, (len(bad), tuple(bad[0]), got[tuple(bad[0])], zr[tuple(bad[0])])
+
+
+@pytest.mark.parametrize("n0,mid,group,n1", [(4096, 4096, 128, 4096), (32768, 8192, 128, 2048)])
+def test_quant_dot_many_columns_full_size_sampled(n0, mid, group, n1):
+    """The weight-like 4096 x 4096 weight with 4096 activation columns and the 32768 x 8192
+    weight with 2048 columns (the bench's prefill cases), in the launch configuration the
+    bench times: every output of 24 sampled rows x 40 sampled columns (the first and last
+    rows and columns among them) against the oracle."""
+    import precision_quantization_gb300 as qz
+    torch = torch_mod()
+    rng = np.random.default_rng(1030 + n0)
+    ng = mid // group
+    codes = rng.integers(0, 2 ** 32, (n0, mid // 8), dtype=np.uint64).astype(np.uint32)
+    sc = (rng.standard_normal((n0, ng)) * 0.02).astype(np.float32)
+    sh = rng.integers(0, 2 ** 32, (n0, (ng + 7) // 8), dtype=np.uint64).astype(np.uint32)
+    y = W.bf16_bits(W.normal(mid, n1, 1.0, seed=1031 + n0, dtype="f32"))
+    z = qz.quant_dot(torch.from_numpy(codes.view(np.int32)).cuda(), torch.from_numpy(sc).cuda(),
+                     torch.from_numpy(sh.view(np.int32)).cuda(), group,
+                     torch.from_numpy(y.view(np.int16)).cuda().view(torch.bfloat16))
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([[0, n0 - 1], rng.integers(0, n0, 22)]))
+    cols = np.unique(np.concatenate([[0, n1 - 1], rng.integers(0, n1, 38)]))
+    zr, za = O.quant_dot(codes[rows], sc[rows], sh[rows], np.ascontiguousarray(y[:, cols]), group)
+    got = z[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()].cpu().numpy()
+    tol = qdot_tolerance(mid, group, za)
+    assert np.all(np.abs(got.astype(np.float64) - zr) <= tol)
