@@ -67,8 +67,9 @@ def measured_peaks() -> dict:
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
-    return {"hbm_gbs": 6800.0, "source": "fallback"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured",
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", 1700.0))}
+    return {"hbm_gbs": 6800.0, "source": "fallback", "bf16_tflops_sustained": 1700.0}
 
 
 def recorded_traffic(kernel: str):
@@ -162,10 +163,10 @@ MATRIX = [
     (1, None, [("int8", "tensor"), ("e4m3", "tensor"), ("mxfp4", "block"), ("nvfp4", "block")]),
     (2, None, [("int8", "row"), ("e4m3", "row"), ("mxfp4", "block"), ("nvfp4", "block"),
                ("int4", "block", 128), ("asym4", "group", 128), ("qdot", "group", 128, 1),
-               ("qdot", "group", 128, 8)]),
+               ("qdot", "group", 128, 8), ("qdot", "group", 128, 4096)]),
     (3, None, [("e4m3", "row"), ("e5m2", "row"), ("nvfp4", "block"), ("nvfp4", "block", "delayed")]),
     (4, None, [("mxfp4", "block"), ("nvfp4", "block"), ("nvfp4", "block", "delayed"),
-               ("int4", "block", 32), ("qdot", "group", 128, 8)]),
+               ("int4", "block", 32), ("qdot", "group", 128, 8), ("qdot", "group", 128, 2048)]),
     (5, None, [(f, g) for f in ("int8", "e4m3", "e5m2") for g in ("unit", "tensor")] +
               [(f, g) for f in ("mxfp4", "nvfp4") for g in ("unit", "block")] +
               [("e4m3", "tensor", "delayed"), ("nvfp4", "block", "delayed")]),
@@ -352,11 +353,17 @@ def measure_qdot(name, n0, mid, group, n1, timed, peaks, dev) -> dict:
         assert rc == 0, rc
     ms = timed(run)
     nb = (w.numel() + sc.numel() + sh.numel()) * 4 + y.numel() * 2 + z.numel() * 4
-    return {"workload": name, "format": "qdot", "granularity": f"group {group} n1 {n1}",
-            "quantize_us": None, "quantize_gbs": None, "quantize_frac": None,
-            "quantize_launches": 0,
-            "dequantize_us": round(ms * 1e3, 1), "dequantize_gbs": round(nb / ms / 1e6, 1),
-            "dequantize_frac": round(nb / ms / 1e6 / peaks["hbm_gbs"], 3)}
+    row = {"workload": name, "format": "qdot", "granularity": f"group {group} n1 {n1}",
+           "quantize_us": None, "quantize_gbs": None, "quantize_frac": None,
+           "quantize_launches": 0,
+           "dequantize_us": round(ms * 1e3, 1), "dequantize_gbs": round(nb / ms / 1e6, 1),
+           "dequantize_frac": round(nb / ms / 1e6 / peaks["hbm_gbs"], 3)}
+    if n1 > 8:  # a dense contraction: tensor throughput against the sustained bf16 peak
+        tf = 2.0 * n0 * mid * n1 / (ms * 1e-3) / 1e12
+        row.update({"tflops": round(tf, 1), "tflops_peak": peaks["bf16_tflops_sustained"],
+                    "tflops_frac": round(tf / peaks["bf16_tflops_sustained"], 3),
+                    "bound": "tensor", "dtype": "bf16 operands, fp32 accumulation"})
+    return row
 
 
 def dist_setup():
