@@ -15,23 +15,27 @@
 // One CTA per SM, persistent over work items (a tile of 128 weight rows x up to 256
 // activation columns, times one slice of l when the tiles are too few to fill the GPU).
 // Roles (warp-specialised, every wait bounded in time):
-//   warp 0        lane 0 streams each 64-wide l-step into a ring of kStages shared-memory
-//                 stages by TMA: the tile's 128 x 8 code words and up to four 64 x 64 bf16
-//                 boxes of y (128-byte swizzle, activation columns contiguous: the MMA's
-//                 "MN-major" B operand).  The warp also owns the tensor-memory allocation.
+//   warp 0        lane 0 streams each 64-wide l-step of y into a ring of kYStages shared-
+//                 memory stages by TMA: up to four 64 x 64 bf16 boxes (128-byte swizzle,
+//                 activation columns contiguous: the MMA's "MN-major" B operand).  The warp
+//                 also owns the tensor-memory allocation.
 //   warp 1        lane 0 issues the MMAs: four 128 x N x 16 steps per stage into one of two
 //                 tensor-memory buffers of 256 fp32 columns, a new buffer at every group
 //                 boundary (and every 1024 values of a longer group), commits each stage's
-//                 completion to its "empty" barrier and each finished group to "P full".
-//   warps 2-3     decode: each thread takes two weight rows of the stage, turns every code
-//                 word into eight bf16 values w - sh (nibbles split by mask, paired by a
-//                 byte permute, OR-ed into bf16 128 + w, one bf16x2 add of -(128 + sh)) and
-//                 stores them in the MMA's K-major 128-byte swizzled layout, then signals
-//                 "A full".
+//                 completion to the "empty" barriers of both rings and each finished group
+//                 to "P full".
+//   warps 2-3     decode: each thread takes two weight rows; it copies their code words
+//                 itself (cp.async, kRawAhead stages ahead), turns every word into eight
+//                 bf16 values w - sh (nibbles split by mask, paired by a byte permute,
+//                 OR-ed into bf16 128 + w, one bf16x2 add of -(128 + sh)) and stores them
+//                 in a ring of kAStages stages in the MMA's K-major 128-byte swizzled
+//                 layout, then signals "A full".  The decoders run ahead of the MMAs
+//                 independently of the activation copies, so the MMA warp's loop waits on
+//                 the TMA ring alone.
 //   warps 4-19    epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. + 31 (its rows)
 //                 and 64 of the 256 columns; for every finished group it adds sc * P into
 //                 64 fp32 registers, frees the buffer, and at the end of the item stores z
-//                 (atomic adds when the item is one slice of several).
+//                 (16-byte stores, or reductions when the item is one slice of several).
 #include <cuda.h>  // CUtensorMap and its enumerators (types only; the encoder is looked up)
 #include <cudaTypedefs.h>
 
@@ -48,25 +52,29 @@ namespace {
 constexpr int kBM = 128;        // weight rows per tile (MMA M, tensor-memory lanes)
 constexpr int kBN = 256;        // activation columns per tile (MMA N at most)
 constexpr int kBK = 64;         // l per stage (one 128-byte swizzle row of bf16)
-constexpr int kStages = 4;
+constexpr int kYStages = 5;     // activation boxes in flight (TMA ring)
+constexpr int kAStages = 3;     // decoded weight stages (decoder ring)
+constexpr int kRawAhead = 3;    // code-word stages a decoder copies ahead of its decoding
+constexpr int kRawStages = kRawAhead + 1;
 constexpr int kDecWarps = 2;
 constexpr int kEpiWarps = 16;
 constexpr int kFirstDec = 2, kFirstEpi = kFirstDec + kDecWarps;
 constexpr int kWarpsTc = kFirstEpi + kEpiWarps;  // 20
 constexpr int kThreadsTc = 32 * kWarpsTc;        // 640
 constexpr uint32_t kSlabBytes = 64 * kBK * 2;    // one 64-column box of y: 8 KiB
-constexpr uint32_t kBBytes = 4 * kSlabBytes;     // 32 KiB
+constexpr uint32_t kYBytes = 4 * kSlabBytes;     // 32 KiB
 constexpr uint32_t kABytes = kBM * kBK * 2;      // 16 KiB of decoded bf16 weights
 constexpr uint32_t kRawBytes = kBM * kBK / 2;    // 4 KiB of code words
-constexpr uint32_t kStageBytes = kBBytes + kABytes + kRawBytes;  // 52 KiB, a multiple of 1 KiB
-constexpr uint32_t kSmemTc = kStages * kStageBytes + 1024;       // + alignment slack
+constexpr uint32_t kAOff = kYStages * kYBytes;   // multiples of 1 KiB
+constexpr uint32_t kRawOff = kAOff + kAStages * kABytes;
+constexpr uint32_t kSmemTc = kRawOff + kRawStages * kRawBytes + 1024;  // + alignment slack
 constexpr int kPieceCap = 1024;  // values of one group accumulated per tensor-memory buffer
 constexpr uint32_t kTmemCols = 512;  // two buffers of 256 fp32 columns
 constexpr uint64_t kTcWaitNs = 1000000000ull;  // 1 s: far beyond any step's latency
 
 struct TcParams {
   CUtensorMap tmap_y;  // bf16 y [mid rows][n1 columns], box 64 x 64, 128-byte swizzle
-  CUtensorMap tmap_w;  // uint32 w [n0 rows][mid / 8 words], box 8 x 128
+  const uint32_t* w;
   const float* scales;
   const uint32_t* shifts;
   float* z;
@@ -164,29 +172,52 @@ __device__ __forceinline__ Item item_of(const TcParams& p, int it) {
   r.nslab = min(4, (p.n1 - r.nb + 63) / 64);
   return r;
 }
-// does a new accumulation piece start at l (a multiple of 16, inside the item's range)?
-__device__ __forceinline__ bool piece_start(int l, int l_begin, int group) {
-  return l == l_begin || l % group == 0 || (group > kPieceCap && l % kPieceCap == 0);
+
+__device__ __forceinline__ void cp_async16_tc(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
+
+// Walks the (item, stage) sequence of one CTA.
+struct Cursor {
+  int it, st, nst;
+  bool valid;
+  __device__ __forceinline__ void start(const TcParams& p, int first) {
+    it = first;
+    st = 0;
+    valid = it < p.items;
+    nst = valid ? item_of(p, it).nst : 0;
+  }
+  __device__ __forceinline__ void next(const TcParams& p, int step) {
+    if (++st < nst) return;
+    it += step;
+    st = 0;
+    valid = it < p.items;
+    nst = valid ? item_of(p, it).nst : 0;
+  }
+};
 
 __global__ void __launch_bounds__(kThreadsTc, 1) quant_dot_tc_kernel(const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t tc_smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[kStages], afull_bar[kStages], empty_bar[kStages];
+  __shared__ __align__(8) uint64_t yfull_bar[kYStages], yempty_bar[kYStages];
+  __shared__ __align__(8) uint64_t afull_bar[kAStages], aempty_bar[kAStages];
   __shared__ __align__(8) uint64_t pfull_bar[2], pempty_bar[2], drain_bar;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t base = (smem_addr(tc_smem_raw) + 1023u) & ~1023u;  // 1 KiB-aligned stages
-  const auto b_of = [&](int s) { return base + static_cast<uint32_t>(s) * kStageBytes; };
-  const auto a_of = [&](int s) { return b_of(s) + kBBytes; };
-  const auto raw_of = [&](int s) { return b_of(s) + kBBytes + kABytes; };
+  const auto y_of = [&](int s) { return base + static_cast<uint32_t>(s) * kYBytes; };
+  const auto a_of = [&](int s) { return base + kAOff + static_cast<uint32_t>(s) * kABytes; };
+  const auto raw_of = [&](int s) { return base + kRawOff + static_cast<uint32_t>(s) * kRawBytes; };
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_addr(&full_bar[s]), 1);
+    for (int s = 0; s < kYStages; ++s) {
+      mbar_init(smem_addr(&yfull_bar[s]), 1);
+      mbar_init(smem_addr(&yempty_bar[s]), 1);
+    }
+    for (int s = 0; s < kAStages; ++s) {
       mbar_init(smem_addr(&afull_bar[s]), kDecWarps);
-      mbar_init(smem_addr(&empty_bar[s]), 1);
+      mbar_init(smem_addr(&aempty_bar[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_addr(&pfull_bar[b]), 1);
@@ -209,119 +240,146 @@ __global__ void __launch_bounds__(kThreadsTc, 1) quant_dot_tc_kernel(const __gri
   const int first_item = blockIdx.x, item_step = gridDim.x;
 
   if (warp == 0) {
-    // ---------------- TMA producer (the whole warp waits; lane 0 issues) ----------------
-    int stage = 0;
-    uint32_t phase = 0;
-    int inflight = 0;  // stages issued and not yet known to have landed (for the drain)
-    for (int it = first_item; it < p.items && !s_abort; it += item_step) {
-      const Item I = item_of(p, it);
-      for (int st = 0; st < I.nst; ++st) {
-        if (!__all_sync(kFull, tc_wait(smem_addr(&empty_bar[stage]), phase ^ 1u, &s_abort))) break;
-        if (lane == 0) {
-          const uint32_t fb = smem_addr(&full_bar[stage]);
+    // ---------------- TMA producer of the activation ring: lane 0 alone ----------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int inflight = 0;  // stages issued and not yet known to have landed (for the drain)
+      for (int it = first_item; it < p.items && !s_abort; it += item_step) {
+        const Item I = item_of(p, it);
+        for (int st = 0; st < I.nst; ++st) {
+          if (!tc_wait(smem_addr(&yempty_bar[stage]), phase ^ 1u, &s_abort)) break;
+          const uint32_t fb = smem_addr(&yfull_bar[stage]);
           const int l0 = (I.st0 + st) * kBK;
-          mbar_expect_tx(fb, kRawBytes + kSlabBytes * static_cast<uint32_t>(I.nslab));
-          tma_load_2d(raw_of(stage), &p.tmap_w, l0 / 8, I.m0, fb);
+          mbar_expect_tx(fb, kSlabBytes * static_cast<uint32_t>(I.nslab));
           for (int sl = 0; sl < I.nslab; ++sl)
-            tma_load_2d(b_of(stage) + sl * kSlabBytes, &p.tmap_y, I.nb + 64 * sl, l0, fb);
-        }
-        __syncwarp();
-        inflight = min(inflight + 1, kStages);
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
+            tma_load_2d(y_of(stage) + sl * kSlabBytes, &p.tmap_y, I.nb + 64 * sl, l0, fb);
+          inflight = min(inflight + 1, kYStages);
+          if (++stage == kYStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
       }
-    }
-    if (s_abort && lane == 0) {
-      // let the copies already issued land before the shared memory is released: the
-      // last `inflight` stages before `stage` (bounded waits; a timeout just ends it)
-      for (int k = 1; k <= inflight; ++k) {
-        const int s = (stage - k + kStages) % kStages;
-        const uint32_t ph = (stage - k < 0) ? (phase ^ 1u) : phase;
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(smem_addr(&full_bar[s]), ph) && globaltimer_ns() - t0 < kTcWaitNs) {
+      if (s_abort) {
+        // let the copies already issued land before the shared memory is released: the
+        // last `inflight` stages before `stage` (bounded waits; a timeout just ends it)
+        for (int k = 1; k <= inflight; ++k) {
+          const int s = (stage - k + kYStages) % kYStages;
+          const uint32_t ph = (stage - k < 0) ? (phase ^ 1u) : phase;
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(smem_addr(&yfull_bar[s]), ph) && globaltimer_ns() - t0 < kTcWaitNs) {
+          }
         }
       }
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ---------------- MMA issuer (the whole warp waits; lane 0 issues) ----------------
-    int stage = 0, buf = 0;
-    uint32_t phase = 0, pe_bits = 3u;  // bit b: parity of the next wait on "P empty" b
-    bool issued = false;
-    for (int it = first_item; it < p.items && !s_abort; it += item_step) {
-      const Item I = item_of(p, it);
-      const uint32_t idesc = idesc_bf16(64 * I.nslab);
-      const int l_begin = I.st0 * kBK;
-      bool open = false, acc = false;
-      for (int st = 0; st < I.nst; ++st) {
-        if (!__all_sync(kFull, tc_wait(smem_addr(&full_bar[stage]), phase, &s_abort))) break;
-        if (!__all_sync(kFull, tc_wait(smem_addr(&afull_bar[stage]), phase, &s_abort))) break;
-        tc_fence_after();
-        const int l0 = (I.st0 + st) * kBK;
-        bool ok = true;
-#pragma unroll
-        for (int j = 0; j < kBK / 16; ++j) {
-          const int l = l0 + 16 * j;
-          if (piece_start(l, l_begin, p.group)) {
-            if (open) {
-              if (lane == 0) tc_commit(smem_addr(&pfull_bar[buf]));
-              __syncwarp();
-              buf ^= 1;
-            }
-            if (!__all_sync(kFull, tc_wait(smem_addr(&pempty_bar[buf]), (pe_bits >> buf) & 1u, &s_abort))) {
-              ok = false;
-              break;
-            }
-            pe_bits ^= 1u << buf;
-            tc_fence_after();
-            open = true;
-            acc = false;
-          }
+    // ---------------- MMA issuer: lane 0 alone, the rest of the warp waits at the end ----
+    // An MMA is taken by the tensor core only when the one before it has started, so
+    // the loop keeps the instructions between two MMAs to a few adds: the piece
+    // boundaries come from a countdown of 16-wide steps, one division per piece.
+    if (lane == 0) {
+      int ys = 0, as = 0, buf = 0;
+      uint32_t yph = 0, aph = 0, pe_bits = 3u;  // bit b: parity of the next wait on "P empty" b
+      bool issued = false;
+      for (int it = first_item; it < p.items && !s_abort; it += item_step) {
+        const Item I = item_of(p, it);
+        const uint32_t idesc = idesc_bf16(64 * I.nslab);
+        const int l_end = (I.st0 + I.nst) * kBK;
+        int l = I.st0 * kBK;
+        int left = 0;  // 16-wide steps of the open piece still to come (0: a new piece starts)
+        bool open = false, acc = false, ok = true;
+        for (int st = 0; st < I.nst && ok; ++st) {
+          if (!tc_wait(smem_addr(&yfull_bar[ys]), yph, &s_abort)) break;
+          if (!tc_wait(smem_addr(&afull_bar[as]), aph, &s_abort)) break;
+          tc_fence_after();
           // A: rows of 128 bytes, 8-row groups 1 KiB apart, +32 bytes per 16 values of l;
           // B: 64-column boxes 8 KiB apart, 8-row groups of l 1 KiB apart, +2 KiB per 16 l
-          if (lane == 0) {
-            const uint64_t ad = smem_desc_sw128(a_of(stage) + 32u * j, 16u, 1024u);
-            const uint64_t bd = smem_desc_sw128(b_of(stage) + 2048u * j, kSlabBytes, 1024u);
-            tc_mma(tmem + static_cast<uint32_t>(buf) * kBN, ad, bd, idesc, acc);
+          const uint64_t ad0 = smem_desc_sw128(a_of(as), 16u, 1024u);
+          const uint64_t bd0 = smem_desc_sw128(y_of(ys), kSlabBytes, 1024u);
+#pragma unroll
+          for (int j = 0; j < kBK / 16; ++j, l += 16) {
+            if (left == 0) {  // a new piece: the end of its group (and of each 1024 values)
+              if (open) {
+                tc_commit(smem_addr(&pfull_bar[buf]));
+                buf ^= 1;
+              }
+              if (!tc_wait(smem_addr(&pempty_bar[buf]), (pe_bits >> buf) & 1u, &s_abort)) {
+                ok = false;
+                break;
+              }
+              pe_bits ^= 1u << buf;
+              tc_fence_after();
+              int nxt = min(l_end, (l / p.group + 1) * p.group);
+              if (p.group > kPieceCap) nxt = min(nxt, (l / kPieceCap + 1) * kPieceCap);
+              left = (nxt - l) / 16;
+              open = true;
+              acc = false;
+            }
+            tc_mma(tmem + static_cast<uint32_t>(buf) * kBN, ad0 + 2u * j, bd0 + 128u * j, idesc, acc);
+            acc = true;
+            issued = true;
+            --left;
           }
-          __syncwarp();
-          acc = true;
-          issued = true;
+          if (!ok) break;
+          tc_commit(smem_addr(&yempty_bar[ys]));  // both stages are free once these MMAs have read them
+          tc_commit(smem_addr(&aempty_bar[as]));
+          if (++ys == kYStages) {
+            ys = 0;
+            yph ^= 1u;
+          }
+          if (++as == kAStages) {
+            as = 0;
+            aph ^= 1u;
+          }
         }
-        if (!ok) break;
-        if (lane == 0) tc_commit(smem_addr(&empty_bar[stage]));
-        __syncwarp();
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
+        if (s_abort || !ok) break;
+        if (open) {
+          tc_commit(smem_addr(&pfull_bar[buf]));
+          buf ^= 1;
         }
       }
-      if (s_abort) break;
-      if (open) {
-        if (lane == 0) tc_commit(smem_addr(&pfull_bar[buf]));
-        __syncwarp();
-        buf ^= 1;
-      }
-    }
-    if (issued && lane == 0) {  // every MMA issued has completed before tensor memory is released
-      tc_commit(smem_addr(&drain_bar));
-      const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(smem_addr(&drain_bar), 0u) && globaltimer_ns() - t0 < kTcWaitNs) {
+      if (issued) {  // every MMA issued has completed before tensor memory is released
+        tc_commit(smem_addr(&drain_bar));
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(smem_addr(&drain_bar), 0u) && globaltimer_ns() - t0 < kTcWaitNs) {
+        }
       }
     }
     __syncwarp();
   } else if (warp < kFirstEpi) {
     // ---------------- decoders: code words -> bf16 (w - sh), swizzled K-major ----------------
-    // Each thread keeps, for each of its two rows, the shift word of its current group and
-    // the one after it in registers: the next word is loaded as soon as the current one is
-    // taken, at least eight groups before it is needed, so no global load latency sits
-    // on the path of a stage.
+    // Each thread owns two rows of every stage.  It copies their code words itself
+    // (cp.async, kRawAhead stages ahead, into its own slots of a small ring: no other
+    // thread touches them, so its own wait_group is the only synchronisation), keeps the
+    // shift word of the current group and the one after it in registers, and fills the
+    // decoded-weight ring, which the MMA warp frees stage by stage.
     const int dt = tid - 32 * kFirstDec;  // 0 .. 63: rows dt and dt + 64 of the tile
-    int stage = 0;
-    uint32_t phase = 0;
-    const int wpg = p.group / 8;  // code words per group (group % 16 == 0)
+    const int wpr = p.mid / 8;
+    const int wpg = p.group / 8;          // code words per group (group % 16 == 0)
+    Cursor pre;                           // the stage whose code words are copied next
+    pre.start(p, first_item);
+    const auto issue_raw = [&](int slot) {
+      if (pre.valid) {
+        const Item J = item_of(p, pre.it);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int r = dt + 64 * h, row = J.m0 + r;
+          if (row < p.n0) {
+            const uint32_t* src = p.w + static_cast<int64_t>(row) * wpr + (J.st0 + pre.st) * (kBK / 8);
+            cp_async16_tc(raw_of(slot) + 32u * r, src);
+            cp_async16_tc(raw_of(slot) + 32u * r + 16u, src + 4);
+          }
+        }
+        pre.next(p, item_step);
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");  // empty groups keep the count uniform
+    };
+#pragma unroll
+    for (int k = 0; k < kRawAhead; ++k) issue_raw(k);
+    int f = 0, as = 0;
+    uint32_t aph = 0;
     for (int it = first_item; it < p.items && !s_abort; it += item_step) {
       const Item I = item_of(p, it);
       int widx[2];
@@ -335,18 +393,32 @@ __global__ void __launch_bounds__(kThreadsTc, 1) quant_dot_tc_kernel(const __gri
         wcur[h] = row < p.n0 ? __ldg(sr + widx[h]) : 0u;
         wnxt[h] = (row < p.n0 && widx[h] + 1 < p.sw) ? __ldg(sr + widx[h] + 1) : 0u;
       }
-      for (int st = 0; st < I.nst; ++st) {
-        if (!__all_sync(kFull, tc_wait(smem_addr(&full_bar[stage]), phase, &s_abort))) break;
+      bool ok = true;
+      for (int st = 0; st < I.nst; ++st, ++f) {
+        issue_raw((f + kRawAhead) % kRawStages);
+        asm volatile("cp.async.wait_group %0;" ::"n"(kRawAhead) : "memory");  // stage f's words are in
+        const uint32_t raw = raw_of(f % kRawStages);
+        if (!__all_sync(kFull, tc_wait(smem_addr(&aempty_bar[as]), aph ^ 1u, &s_abort))) {
+          ok = false;
+          break;
+        }
         const int w0 = (I.st0 + st) * (kBK / 8);  // first code word of the stage in the row
         const int g0 = w0 / wpg, left0 = (g0 + 1) * wpg - w0;  // its group, words left in it
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int r = dt + 64 * h;
           const int row = I.m0 + r;
-          const uint4 c0 = lds128_tc(raw_of(stage) + 32u * r);
-          const uint4 c1 = lds128_tc(raw_of(stage) + 32u * r + 16u);
-          const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-          const uint32_t arow = a_of(stage) + 128u * r;
+          uint32_t cw[8];
+          if (row < p.n0) {
+            const uint4 c0 = lds128_tc(raw + 32u * r);
+            const uint4 c1 = lds128_tc(raw + 32u * r + 16u);
+            cw[0] = c0.x; cw[1] = c0.y; cw[2] = c0.z; cw[3] = c0.w;
+            cw[4] = c1.x; cw[5] = c1.y; cw[6] = c1.z; cw[7] = c1.w;
+          } else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) cw[c] = 0u;
+          }
+          const uint32_t arow = a_of(as) + 128u * r;
           int g = g0, left = left0;  // group of word c, and its words still to come
           uint32_t addc = 0u;        // bf16 pair (-(128 + sh), -(128 + sh)) of group g
 #pragma unroll
@@ -384,13 +456,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1) quant_dot_tc_kernel(const __gri
         }
         fence_proxy_async();  // generic-proxy stores -> visible to the tensor cores
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&afull_bar[stage]));
-        if (++stage == kStages) {
-          stage = 0;
-          phase ^= 1u;
+        if (lane == 0) mbar_arrive(smem_addr(&afull_bar[as]));
+        if (++as == kAStages) {
+          as = 0;
+          aph ^= 1u;
         }
       }
+      if (!ok) break;
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");  // no copy of this thread is left in flight
   } else {
     // ---------------- epilogue ----------------
     const int q = warp & 3;                 // tensor-memory lane quarter of this warp
@@ -525,15 +599,6 @@ qz_status launch_quant_dot_tc(const uint32_t* w, const float* scales, const uint
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return QZ_ERR_CUDA;
   }
-  {  // w: dimension 0 = code words of a row, dimension 1 = rows
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(mid / 8), static_cast<cuuint64_t>(n0)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(mid / 8) * 4};
-    const cuuint32_t box[2] = {kBK / 8, kBM}, es[2] = {1, 1};
-    if (enc(&p.tmap_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t*>(w), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return QZ_ERR_CUDA;
-  }
   const int sms = sm_count();
   const int64_t tiles_m = (n0 + kBM - 1) / kBM, tiles_n = (n1 + kBN - 1) / kBN;
   const int64_t tiles = tiles_m * tiles_n, stages_total = mid / kBK;
@@ -544,6 +609,7 @@ qz_status launch_quant_dot_tc(const uint32_t* w, const float* scales, const uint
   ksplit = (stages_total + slice_stages - 1) / slice_stages;
   const int64_t items = tiles * ksplit;
   if (items >= (int64_t{1} << 31)) return QZ_ERR_UNSUPPORTED;
+  p.w = w;
   p.scales = scales;
   p.shifts = shifts;
   p.z = z;
