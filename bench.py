@@ -38,6 +38,23 @@ KERNEL_SOURCES = ["precision_quantization_gb300/csrc/qz_device.cuh",
                   "precision_quantization_gb300/csrc/qz_amax.cu"]
 
 
+class L2Flush:
+    """Empties the L2 of the timed workload's data between timed iterations: a write of
+    L2_FLUSH_BYTES (more than the 126 MB L2), then a read of as many other bytes, which
+    writes the first buffer's dirty lines back to DRAM before the timed region starts.
+    Without the read, the next timed kernel would pay for up to 126 MB of the flush's
+    write-back (about 19 us at the copy peak), a cost of the flush, not of the kernel."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty((L2_FLUSH_BYTES,), dtype=torch.uint8, device=dev)
+        self.r = torch.zeros((L2_FLUSH_BYTES // 8,), dtype=torch.int64, device=dev)
+
+    def run(self):
+        self.w.zero_()
+        self.r.max()  # reads every byte of the second buffer
+
+
 def algorithmic_bytes(n: int) -> dict:
     """Bytes in + bytes out per launch, from the formats' layouts (bf16 input and output,
     E2M1 codes 0.5 B/element, one E8M0 byte per 32 / one E4M3 byte per 16 elements, one
@@ -194,7 +211,7 @@ def compact_matrix(rows: list) -> dict:
     return out
 
 
-def measure_matrix(dev, peaks, flush, x4=None, reps=10, which=(1, 2, 3, 4, 5)) -> list:
+def measure_matrix(dev, peaks, flush, x4=None, reps=30, which=(1, 2, 3, 4, 5)) -> list:
     import numpy as np
     import torch
     import precision_quantization_gb300 as qz
@@ -211,7 +228,7 @@ def measure_matrix(dev, peaks, flush, x4=None, reps=10, which=(1, 2, 3, 4, 5)) -
         ts = []
         for _ in range(reps):
             if cold:
-                flush.zero_()
+                flush.run()
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record(stream)
@@ -219,7 +236,10 @@ def measure_matrix(dev, peaks, flush, x4=None, reps=10, which=(1, 2, 3, 4, 5)) -
             b.record(stream)
             torch.cuda.synchronize(dev)
             ts.append(a.elapsed_time(b))
-        return statistics.median(ts)
+        # the mean: the event clock ticks in steps of about 2 us here, too coarse for the
+        # 5-50 us launches of the smaller workloads, and the mean over many launches with
+        # varying start phases is not biased by the step the way a median is
+        return statistics.mean(ts)
 
     for k, rows, runs in MATRIX:
         if k not in which:
@@ -551,7 +571,7 @@ def main():
     dev = torch.device("cuda", local)
     which = tuple(int(v) for v in args.matrix_workloads.split(",") if v)
     if args.matrix_only:
-        flush = torch.empty((L2_FLUSH_BYTES,), dtype=torch.uint8, device=dev)
+        flush = L2Flush(dev)
         m = measure_matrix(dev, measured_peaks(), flush, which=which)
         print(json.dumps({"metric": METRIC, "unit": "GB/s", "formats": m}), flush=True)
         return
@@ -569,7 +589,7 @@ def main():
     ys = {f: torch.empty((rows, COLS), dtype=torch.bfloat16, device=dev) for f in outs}
     sts = {f: torch.empty((qz.STATS_BYTES,), dtype=torch.uint8, device=dev) for f in outs}
     amax_buf = torch.empty((1,), dtype=torch.float32, device=dev)
-    flush = torch.empty((L2_FLUSH_BYTES,), dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
     desc = {f: qz.make_desc(f, qz.QZ_BF16, qz.QZ_GRAN_BLOCK, rows, COLS) for f in outs}
@@ -605,7 +625,7 @@ def main():
 
     clk = ClockSampler(local).__enter__()
     for _ in range(args.warmup):
-        flush.zero_()
+        flush.run()
         launches(x.data_ptr())
     torch.cuda.synchronize(dev)
     if ws.status() != 0:
@@ -618,7 +638,7 @@ def main():
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
     for k in range(args.steps):
-        flush.zero_()  # L2 flush between timed steps (outside the events)
+        flush.run()  # L2 flush between timed steps (outside the events)
         launches(x.data_ptr(), evs[k])
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - t0
@@ -660,7 +680,7 @@ def main():
             plan.run(xh)
         e_ms = []
         for _ in range(args.e2e_steps):
-            flush.zero_()
+            flush.run()
             torch.cuda.synchronize(dev)
             t1 = time.perf_counter()
             plan.run(xh)
@@ -704,7 +724,8 @@ def main():
                    "step": "mx quantize(+stats)->dequantize(bf16); nv amax->quantize(+stats)"
                            "->dequantize(bf16)",
                    "bytes_per_step": step_bytes,
-                   "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write); "
+                   "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, then "
+                         f"{L2_FLUSH_BYTES >> 20} MiB read to write its dirty lines back); "
                          "input 512 MiB > L2",
                    "parallelism": f"replicas x{world}"},
         "elements_per_s": round(n * 2 * world / (ms * 1e-3), 1),

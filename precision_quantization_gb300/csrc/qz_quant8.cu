@@ -644,6 +644,104 @@ __global__ void __launch_bounds__(kThreads) quant8_rowwarp_kernel(Q8Args a, floa
   if constexpr (STATS) stats_finish(acc, a.ws, a.stats, static_cast<uint64_t>(g.rows * g.cols));
 }
 
+// Per-row scale with the fused statistics, rows of at most kRowSlotMaxBytes: one warp per
+// row and a shared-memory slot per warp.  Lane 0 brings the row in with one bulk copy (on
+// the warp's own barrier), the warp takes the row amax from the slot, then quantizes the
+// row chunk by chunk from the slot with the statistics -- a loop that is not unrolled, so
+// the chunk code exists once per variant of the relative-error search.  Warps never wait
+// for one another, so the per-row latency of one warp overlaps with the work of the rest.
+constexpr int kRowSlotMaxBytes = 16 * 1024;
+
+template <int FMT, int DT>
+__global__ void __launch_bounds__(kThreads) quant8_rowslot_kernel(Q8Args a, float zero, uint32_t slot_bytes) {
+  constexpr int EPC = Elem<DT>::kPer32B;
+  constexpr int NP = EPC / 2;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bars[kWarps];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const Geom& g = a.g;
+  const uint32_t row_bytes = static_cast<uint32_t>(g.cols) * Elem<DT>::kBytes;  // whole chunks
+  if (a.tscale_out && blockIdx.x == 0 && tid == 0) *a.tscale_out = 1.0f;
+  const uint32_t bar = smem_addr(&bars[warp]);
+  const uint32_t slot = smem_addr(smem) + static_cast<uint32_t>(warp) * slot_bytes;
+  if (lane == 0) {
+    mbar_init(bar, 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
+  const uint64_t z2 = pk(zero, zero);
+  StatAcc acc;
+  uint32_t am_unused = 0u, phase = 0u;
+  const int cpr = static_cast<int>(g.cpr);
+  const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
+  for (int64_t row = static_cast<int64_t>(blockIdx.x) * kWarps + warp; row < g.rows; row += nwarps) {  // warp-uniform
+    if (lane == 0) {
+      mbar_expect_tx(bar, row_bytes);
+      bulk_g2s(slot, static_cast<const char*>(a.x) + row * g.ld * Elem<DT>::kBytes, row_bytes, bar);
+    }
+    if (!__all_sync(kFull, mbar_wait(bar, phase, kWaitLimitNs))) {
+      // the copy did not land within the limit: flag it, let it land (bounded), stop
+      if (lane == 0) {
+        flag_status(a.ws, QZ_FLAG_PIPELINE_TIMEOUT);
+        mbar_wait(bar, phase, kWaitLimitNs);
+      }
+      __syncwarp();
+      break;
+    }
+    phase ^= 1u;
+    // pass 1: row amax (NaN propagates)
+    float A = 0.0f;
+#pragma unroll 1
+    for (int j = lane; j < cpr; j += 32) {
+      uint32_t w[8];
+      lds32B(w, slot + 32u * static_cast<uint32_t>(j));
+      if constexpr (DT == QZ_BF16) {
+        A = absmax_nan(A, bf16x16_absmax(w));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) A = absmax3(A, __uint_as_float(w[i]), __uint_as_float(w[i + 1]));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) A = absmax_nan(A, __shfl_xor_sync(kFull, A, o));
+    float s = __fdiv_rn(A, Fmt8<FMT>::kMax);  // alpha / qmax
+    if (s == 0.0f) s = 1.0f;
+    const float r = __frcp_rn(s);
+    const bool fast = fast_div_ok(s);
+    if (lane == 0) {
+      a.scales[row] = s;
+      if (!is_finite_f(A)) flag_status(a.ws, QZ_FLAG_NONFINITE_INPUT);
+    }
+    const uint64_t r2 = pk(r, r), ns2 = pk(-s, -s), s2 = pk(s, s);
+    // pass 2: codes and statistics, one chunk per lane per step (warp-uniform trip count:
+    // the relative-error search votes)
+    float tpart = 0.0f;
+    uint8_t* crow = a.codes + row * g.cols;
+#pragma unroll 1
+    for (int jb = 0; jb < cpr; jb += 32) {
+      const int j = jb + lane;
+      const bool valid = j < cpr;
+      uint32_t w[8];
+      if (valid) {
+        lds32B(w, slot + 32u * static_cast<uint32_t>(j));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = 0u;
+      }
+      if (acc.T >= 1.0f)
+        q8_chunk<FMT, DT, kTensorComputed, true, false, false>(w, valid, crow + static_cast<int64_t>(j) * EPC, s,
+                                                               r2, ns2, s2, z2, fast, a.ws, acc, tpart, am_unused);
+      else
+        q8_chunk<FMT, DT, kTensorComputed, true, true, false>(w, valid, crow + static_cast<int64_t>(j) * EPC, s,
+                                                              r2, ns2, s2, z2, fast, a.ws, acc, tpart, am_unused);
+    }
+    acc_add_sum(acc, tpart);
+    __syncwarp();  // every lane is done with the slot before the next copy refills it
+  }
+  (void)NP;
+  stats_finish(acc, a.ws, a.stats, static_cast<uint64_t>(g.rows * g.cols));
+}
+
 template <typename K>
 qz_status go(K kern, const Q8Args& args, int64_t work_ctas, cudaStream_t s) {
   const int grid = grid_for(reinterpret_cast<const void*>(kern), work_ctas, s);
@@ -673,6 +771,17 @@ qz_status run_row(const Q8Args& args, cudaStream_t s) {
     if (g.cpr <= 64) return go2(&quant8_rowwarp_kernel<FMT, DT, STATS, 2>, args, work, s);
     if (g.cpr <= 128) return go2(&quant8_rowwarp_kernel<FMT, DT, STATS, 4>, args, work, s);
     return go2(&quant8_rowwarp_kernel<FMT, DT, STATS, 8>, args, work, s);
+  }
+  // with statistics, rows of whole chunks up to 16 KiB: a warp and a shared-memory slot per row
+  if (STATS && g.vec && row_bytes <= kRowSlotMaxBytes && row_bytes % 32 == 0 &&
+      reinterpret_cast<uintptr_t>(args.x) % 16 == 0 && (g.ld * Elem<DT>::kBytes) % 16 == 0) {
+    auto kern = &quant8_rowslot_kernel<FMT, DT>;
+    const uint32_t slot = static_cast<uint32_t>((row_bytes + 127) / 128 * 128);
+    const size_t smem = static_cast<size_t>(kWarps) * slot;
+    if (!set_dyn_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem))) return QZ_ERR_CUDA;
+    const int grid = grid_for(reinterpret_cast<const void*>(kern), (rows + kWarps - 1) / kWarps, s, smem);
+    kern<<<grid, kThreads, smem, s>>>(args, 0.0f, slot);
+    return launch_status();
   }
   if (g.vec && row_bytes <= kRowPipeMaxBytes && reinterpret_cast<uintptr_t>(args.x) % 16 == 0 &&
       (g.ld * Elem<DT>::kBytes) % 16 == 0) {

@@ -313,3 +313,25 @@ def test_named_workload_full_size(k):
         assert g["status"] == 0
         if gran == O.GRAN_ROW:  # the quantize without statistics runs other kernels there
             assert_parity(run_gpu(x, fmt, gran, stats=False, out_dtypes=od), o, stats=False)
+
+
+@pytest.mark.parametrize("fmt", FMT8)
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_parity_row_with_stats_paths(fmt, dtype):
+    """Per-row scales with the fused statistics: rows of whole chunks up to 16 KiB take a
+    warp and a shared-memory slot each; longer rows the row pipeline.  One-chunk rows, many
+    short rows, rows of exactly 16 KiB and just past it, and an odd row count."""
+    eb = 2 if dtype == "bf16" else 4
+    shapes = [(1, 32 // eb), (3000, 64), (77, 4096 + 32), (9, 16384 // eb), (5, 16384 // eb + 32 // eb),
+              (131, 1024)]
+    for i, (r, c) in enumerate(shapes):
+        x = gen(r, c, dtype, seed=1100 + i, kind="edge" if (dtype == "f32" and i % 2) else "lognormal")
+        assert_parity(run_gpu(x, fmt, O.GRAN_ROW), run_oracle(x, fmt, O.GRAN_ROW))
+
+
+def test_row_with_stats_flags_nonfinite():
+    """A NaN in one row of the warp-per-row path raises the non-finite flag."""
+    x = W.lognormal_signed(40, 512, seed=1200, dtype="f32")
+    x[17, 300] = np.float32("nan")
+    g = run_gpu(x, O.E4M3, O.GRAN_ROW, out_dtypes=())
+    assert g["status"] & 0x1
