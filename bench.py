@@ -211,7 +211,7 @@ def compact_matrix(rows: list) -> dict:
     return out
 
 
-def measure_matrix(dev, peaks, flush, x4=None, reps=30, which=(1, 2, 3, 4, 5)) -> list:
+def measure_matrix(dev, peaks, flush, x4=None, reps=30, which=(1, 2, 3, 4, 5), max_rows=None) -> list:
     import numpy as np
     import torch
     import precision_quantization_gb300 as qz
@@ -244,7 +244,9 @@ def measure_matrix(dev, peaks, flush, x4=None, reps=30, which=(1, 2, 3, 4, 5)) -
     for k, rows, runs in MATRIX:
         if k not in which:
             continue
-        if k == 4 and x4 is not None:
+        if max_rows is not None:
+            rows = min(max_rows, W.WORKLOADS[k]["rows"])
+        if k == 4 and x4 is not None and max_rows is None:
             x_np, x = None, x4
         else:
             x_np = W.workload(k, rows=rows)
@@ -552,6 +554,8 @@ def main():
                     help="print only the per-format matrix (one JSON line)")
     ap.add_argument("--matrix-workloads", default="1,2,3,4,5",
                     help="comma-separated workload numbers of the matrix")
+    ap.add_argument("--matrix-rows", type=int, default=None,
+                    help="at most this many rows of each matrix workload (small cases for profiling)")
     ap.add_argument("--rows", type=int, default=ROWS,
                     help="rows of the workload (same recipe); the default is the full size")
     args = ap.parse_args()
@@ -572,7 +576,7 @@ def main():
     which = tuple(int(v) for v in args.matrix_workloads.split(",") if v)
     if args.matrix_only:
         flush = L2Flush(dev)
-        m = measure_matrix(dev, measured_peaks(), flush, which=which)
+        m = measure_matrix(dev, measured_peaks(), flush, which=which, max_rows=args.matrix_rows)
         print(json.dumps({"metric": METRIC, "unit": "GB/s", "formats": m}), flush=True)
         return
     if world > 1:
