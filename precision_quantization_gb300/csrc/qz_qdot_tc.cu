@@ -24,7 +24,8 @@
 //                 boundary (and every 1024 values of a longer group), commits each stage's
 //                 completion to the "empty" barriers of both rings and each finished group
 //                 to "P full".
-//   warps 2-3     decode: each thread takes two weight rows; it copies their code words
+//   warps 2-5     decode (warps 2-3 when groups are shorter than 128): each thread takes one
+//                 (two) weight rows; it copies their code words
 //                 itself (cp.async, kRawAhead stages ahead), turns every word into eight
 //                 bf16 values w - sh (nibbles split by mask, paired by a byte permute,
 //                 OR-ed into bf16 128 + w, one bf16x2 add of -(128 + sh)) and stores them
@@ -32,7 +33,7 @@
 //                 layout, then signals "A full".  The decoders run ahead of the MMAs
 //                 independently of the activation copies, so the MMA warp's loop waits on
 //                 the TMA ring alone.
-//   warps 4-19    epilogue: warp w reads tensor-memory lanes 32 (w % 4) .. + 31 (its rows)
+//   warps 6-21    epilogue (4-19): warp w reads tensor-memory lanes 32 (w % 4) .. + 31 (its rows)
 //                 and 64 of the 256 columns; for every finished group it adds sc * P into
 //                 64 fp32 registers, frees the buffer, and at the end of the item stores z
 //                 (16-byte stores, or reductions when the item is one slice of several).
@@ -56,11 +57,16 @@ constexpr int kYStages = 5;     // activation boxes in flight (TMA ring)
 constexpr int kAStages = 3;     // decoded weight stages (decoder ring)
 constexpr int kRawAhead = 3;    // code-word stages a decoder copies ahead of its decoding
 constexpr int kRawStages = kRawAhead + 1;
-constexpr int kDecWarps = 2;
 constexpr int kEpiWarps = 16;
-constexpr int kFirstDec = 2, kFirstEpi = kFirstDec + kDecWarps;
-constexpr int kWarpsTc = kFirstEpi + kEpiWarps;  // 20
-constexpr int kThreadsTc = 32 * kWarpsTc;        // 640
+constexpr int kFirstDec = 2;
+// Warp layout for D decoder warps (two or four: see quant_dot_tc_kernel)
+template <int D>
+struct TcShape {
+  static constexpr int kDecWarps = D;
+  static constexpr int kDecRows = kBM / (32 * D);  // weight rows per decoder thread
+  static constexpr int kFirstEpi = kFirstDec + D;
+  static constexpr int kThreads = 32 * (kFirstEpi + kEpiWarps);
+};
 constexpr uint32_t kSlabBytes = 64 * kBK * 2;    // one 64-column box of y: 8 KiB
 constexpr uint32_t kYBytes = 4 * kSlabBytes;     // 32 KiB
 constexpr uint32_t kABytes = kBM * kBK * 2;      // 16 KiB of decoded bf16 weights
@@ -196,7 +202,14 @@ struct Cursor {
   }
 };
 
-__global__ void __launch_bounds__(kThreadsTc, 1) quant_dot_tc_kernel(const __grid_constant__ TcParams p) {
+// DEC decoder warps: four keep pace with the MMAs for groups of 128 and more (4096^3 at
+// group 128: 345 -> 296 us); with their 704 threads the epilogue's 64 accumulators spill a
+// little, which costs more than the extra decoders gain when every 16 to 64 values end a
+// group (group 32: 467 -> 715 us, group 64: 392 -> 407 us), so those run with two.
+template <int DEC>
+__global__ void __launch_bounds__(TcShape<DEC>::kThreads, 1) quant_dot_tc_kernel(const __grid_constant__ TcParams p) {
+  constexpr int kDecWarps = TcShape<DEC>::kDecWarps, kDecRows = TcShape<DEC>::kDecRows;
+  constexpr int kFirstEpi = TcShape<DEC>::kFirstEpi;
   extern __shared__ uint8_t tc_smem_raw[];
   __shared__ __align__(8) uint64_t yfull_bar[kYStages], yempty_bar[kYStages];
   __shared__ __align__(8) uint64_t afull_bar[kAStages], aempty_bar[kAStages];
@@ -355,7 +368,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) quant_dot_tc_kernel(const __gri
     // thread touches them, so its own wait_group is the only synchronisation), keeps the
     // shift word of the current group and the one after it in registers, and fills the
     // decoded-weight ring, which the MMA warp frees stage by stage.
-    const int dt = tid - 32 * kFirstDec;  // 0 .. 63: rows dt and dt + 64 of the tile
+    const int dt = tid - 32 * kFirstDec;  // rows dt + 32 kDecWarps h of the tile, h < kDecRows
     const int wpr = p.mid / 8;
     const int wpg = p.group / 8;          // code words per group (group % 16 == 0)
     Cursor pre;                           // the stage whose code words are copied next
@@ -364,8 +377,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) quant_dot_tc_kernel(const __gri
       if (pre.valid) {
         const Item J = item_of(p, pre.it);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int r = dt + 64 * h, row = J.m0 + r;
+        for (int h = 0; h < kDecRows; ++h) {
+          const int r = dt + 32 * kDecWarps * h, row = J.m0 + r;
           if (row < p.n0) {
             const uint32_t* src = p.w + static_cast<int64_t>(row) * wpr + (J.st0 + pre.st) * (kBK / 8);
             cp_async16_tc(raw_of(slot) + 32u * r, src);
@@ -382,12 +395,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1) quant_dot_tc_kernel(const __gri
     uint32_t aph = 0;
     for (int it = first_item; it < p.items && !s_abort; it += item_step) {
       const Item I = item_of(p, it);
-      int widx[2];
-      uint32_t wcur[2], wnxt[2];
+      int widx[kDecRows];
+      uint32_t wcur[kDecRows], wnxt[kDecRows];
       const int gfirst = I.st0 * (kBK / 8) / wpg;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int row = I.m0 + dt + 64 * h;
+      for (int h = 0; h < kDecRows; ++h) {
+        const int row = I.m0 + dt + 32 * kDecWarps * h;
         const uint32_t* sr = p.shifts + static_cast<int64_t>(row < p.n0 ? row : 0) * p.sw;
         widx[h] = gfirst >> 3;
         wcur[h] = row < p.n0 ? __ldg(sr + widx[h]) : 0u;
@@ -405,8 +418,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) quant_dot_tc_kernel(const __gri
         const int w0 = (I.st0 + st) * (kBK / 8);  // first code word of the stage in the row
         const int g0 = w0 / wpg, left0 = (g0 + 1) * wpg - w0;  // its group, words left in it
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int r = dt + 64 * h;
+        for (int h = 0; h < kDecRows; ++h) {
+          const int r = dt + 32 * kDecWarps * h;
           const int row = I.m0 + r;
           uint32_t cw[8];
           if (row < p.n0) {
@@ -625,11 +638,14 @@ qz_status launch_quant_dot_tc(const uint32_t* w, const float* scales, const uint
   p.slice_stages = static_cast<int>(slice_stages);
   p.stages_total = static_cast<int>(stages_total);
   p.items = static_cast<int>(items);
-  if (!set_dyn_smem(reinterpret_cast<const void*>(&quant_dot_tc_kernel), static_cast<int>(kSmemTc)))
-    return QZ_ERR_CUDA;
+  const bool four = group >= 128;
+  const void* kern = four ? reinterpret_cast<const void*>(&quant_dot_tc_kernel<4>)
+                          : reinterpret_cast<const void*>(&quant_dot_tc_kernel<2>);
+  if (!set_dyn_smem(kern, static_cast<int>(kSmemTc))) return QZ_ERR_CUDA;
   if (ksplit > 1 && launch_zero_z(z, ld_z, n0, n1, s) != QZ_OK) return QZ_ERR_CUDA;
   const int grid = static_cast<int>(std::min<int64_t>(items, sms));
-  quant_dot_tc_kernel<<<grid, kThreadsTc, kSmemTc, s>>>(p);
+  if (four) quant_dot_tc_kernel<4><<<grid, TcShape<4>::kThreads, kSmemTc, s>>>(p);
+  else quant_dot_tc_kernel<2><<<grid, TcShape<2>::kThreads, kSmemTc, s>>>(p);
   return launch_status();
 }
 
