@@ -59,14 +59,29 @@ constexpr int kRawAhead = 3;    // code-word stages a decoder copies ahead of it
 constexpr int kRawStages = kRawAhead + 1;
 constexpr int kEpiWarps = 16;
 constexpr int kFirstDec = 2;
-// Warp layout for D decoder warps (two or four: see quant_dot_tc_kernel)
+// Warp layout for D decoder warps (two or four: see quant_dot_tc_kernel).  A warp runs on
+// scheduler (SM sub-partition) warp % 4, and an MMA is slowed by every busy warp that
+// shares the issuing warp's scheduler (measured: 128 cycles per 128 x 256 x 16 MMA alone,
+// 210 with four warps of dependent FMAs beside it, 586 with four warps running a long
+// unrolled body; the same warps on the other three schedulers, or warps polling a barrier,
+// cost nothing).  So no decoder is a warp w with w % 4 == 1, the MMA warp's scheduler: the
+// decoders are the first D warps of [2, kFirstEpi) outside it, and the others idle.  The
+// epilogue warps must cover all four schedulers (a warp reads tensor-memory lanes
+// 32 (w % 4) .. + 31 only), and their work is kept short.
 template <int D>
 struct TcShape {
   static constexpr int kDecWarps = D;
   static constexpr int kDecRows = kBM / (32 * D);  // weight rows per decoder thread
-  static constexpr int kFirstEpi = kFirstDec + D;
+  static constexpr int kFirstEpi = D == 2 ? 4 : 8;
   static constexpr int kThreads = 32 * (kFirstEpi + kEpiWarps);
+  // decoder index of warp w in [2, kFirstEpi), -1 for an idle warp
+  static __device__ __forceinline__ int dec_of(int w) {
+    if ((w & 3) == 1) return -1;
+    const int d = (w - kFirstDec) - (w - kFirstDec) / 4;  // less the warps 5, 9, ... below w
+    return d < D ? d : -1;
+  }
 };
+static_assert(TcShape<2>::kFirstEpi % 4 == 0 && TcShape<4>::kFirstEpi % 4 == 0, "epilogue quarters by warp % 4");
 constexpr uint32_t kSlabBytes = 64 * kBK * 2;    // one 64-column box of y: 8 KiB
 constexpr uint32_t kYBytes = 4 * kSlabBytes;     // 32 KiB
 constexpr uint32_t kABytes = kBM * kBK * 2;      // 16 KiB of decoded bf16 weights
@@ -112,18 +127,29 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t adesc, uint64_t bdes
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc ? 1u : 0u)
       : "memory");
 }
-// 16 consecutive fp32 columns of this thread's tensor-memory lane
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
+// 8 consecutive fp32 columns of this thread's tensor-memory lane, as 4 fp32 pairs (the
+// operands of the packed FMAs of the epilogue; 8 columns at a time keep the epilogue's
+// registers within the 80 a thread has)
+__device__ __forceinline__ void tmem_ld8_pairs(uint32_t taddr, uint64_t (&v)[4]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      "{\n\t.reg .b32 r<8>;\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {r0,r1,r2,r3,r4,r5,r6,r7}, [%4];\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n\t"
+      "mov.b64 %0, {r0, r1};\n\tmov.b64 %1, {r2, r3};\n\tmov.b64 %2, {r4, r5};\n\tmov.b64 %3, {r6, r7};\n\t}"
+      : "=l"(v[0]), "=l"(v[1]), "=l"(v[2]), "=l"(v[3])
       : "r"(taddr)
       : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+// 16 bytes of z from two fp32 pairs: a store, or (a slice of several) a reduction
+__device__ __forceinline__ void st_pairs(float* dst, uint64_t a, uint64_t b) {
+  asm volatile("st.global.v2.b64 [%0], {%1, %2};" ::"l"(dst), "l"(a), "l"(b) : "memory");
+}
+__device__ __forceinline__ void red_pairs(float* dst, uint64_t a, uint64_t b) {
+  asm volatile(
+      "{\n\t.reg .f32 f<4>;\n\tmov.b64 {f0, f1}, %1;\n\tmov.b64 {f2, f3}, %2;\n\t"
+      "red.global.add.v4.f32 [%0], {f0, f1, f2, f3};\n\t}" ::"l"(dst),
+      "l"(a), "l"(b)
+      : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -184,21 +210,32 @@ __device__ __forceinline__ void cp_async16_tc(uint32_t dst, const void* src) {
 }
 
 // Walks the (item, stage) sequence of one CTA.
+// Walks the (item, stage) sequence of one CTA; the item's fields are computed once per item
+// (item_of divides by run-time values).
 struct Cursor {
-  int it, st, nst;
+  int it, st, nst, m0, st0;
   bool valid;
+  __device__ __forceinline__ void load(const TcParams& p) {
+    valid = it < p.items;
+    if (valid) {
+      const Item I = item_of(p, it);
+      nst = I.nst;
+      m0 = I.m0;
+      st0 = I.st0;
+    } else {
+      nst = 0;
+    }
+  }
   __device__ __forceinline__ void start(const TcParams& p, int first) {
     it = first;
     st = 0;
-    valid = it < p.items;
-    nst = valid ? item_of(p, it).nst : 0;
+    load(p);
   }
   __device__ __forceinline__ void next(const TcParams& p, int step) {
     if (++st < nst) return;
     it += step;
     st = 0;
-    valid = it < p.items;
-    nst = valid ? item_of(p, it).nst : 0;
+    load(p);
   }
 };
 
@@ -206,7 +243,13 @@ struct Cursor {
 // group 128: 345 -> 296 us); with their 704 threads the epilogue's 64 accumulators spill a
 // little, which costs more than the extra decoders gain when every 16 to 64 values end a
 // group (group 32: 467 -> 715 us, group 64: 392 -> 407 us), so those run with two.
-template <int DEC>
+//
+// GW: code words per group when a stage's groups sit at fixed places in it -- 8 for every
+// group that is a multiple of 64 values (a stage lies inside one group), 4 for groups of
+// 32, 2 for groups of 16 (2 or 4 whole groups a stage) -- so the decode of a stage is
+// straight-line code; 0 for the other groups (48, 80, ...), whose boundaries move from
+// stage to stage.
+template <int DEC, int GW>
 __global__ void __launch_bounds__(TcShape<DEC>::kThreads, 1) quant_dot_tc_kernel(const __grid_constant__ TcParams p) {
   constexpr int kDecWarps = TcShape<DEC>::kDecWarps, kDecRows = TcShape<DEC>::kDecRows;
   constexpr int kFirstEpi = TcShape<DEC>::kFirstEpi;
@@ -291,7 +334,7 @@ __global__ void __launch_bounds__(TcShape<DEC>::kThreads, 1) quant_dot_tc_kernel
     // ---------------- MMA issuer: lane 0 alone, the rest of the warp waits at the end ----
     // An MMA is taken by the tensor core only when the one before it has started, so
     // the loop keeps the instructions between two MMAs to a few adds: the piece
-    // boundaries come from a countdown of 16-wide steps, one division per piece.
+    // boundaries come from a countdown of 16-wide steps and a running group boundary.
     if (lane == 0) {
       int ys = 0, as = 0, buf = 0;
       uint32_t yph = 0, aph = 0, pe_bits = 3u;  // bit b: parity of the next wait on "P empty" b
@@ -301,6 +344,7 @@ __global__ void __launch_bounds__(TcShape<DEC>::kThreads, 1) quant_dot_tc_kernel
         const uint32_t idesc = idesc_bf16(64 * I.nslab);
         const int l_end = (I.st0 + I.nst) * kBK;
         int l = I.st0 * kBK;
+        int gb = (l / p.group + 1) * p.group;  // the next group boundary after l
         int left = 0;  // 16-wide steps of the open piece still to come (0: a new piece starts)
         bool open = false, acc = false, ok = true;
         for (int st = 0; st < I.nst && ok; ++st) {
@@ -324,8 +368,9 @@ __global__ void __launch_bounds__(TcShape<DEC>::kThreads, 1) quant_dot_tc_kernel
               }
               pe_bits ^= 1u << buf;
               tc_fence_after();
-              int nxt = min(l_end, (l / p.group + 1) * p.group);
+              int nxt = min(l_end, gb);
               if (p.group > kPieceCap) nxt = min(nxt, (l / kPieceCap + 1) * kPieceCap);
+              if (nxt == gb) gb += p.group;
               left = (nxt - l) / 16;
               open = true;
               acc = false;
@@ -361,26 +406,26 @@ __global__ void __launch_bounds__(TcShape<DEC>::kThreads, 1) quant_dot_tc_kernel
       }
     }
     __syncwarp();
-  } else if (warp < kFirstEpi) {
+  } else if (warp < kFirstEpi && TcShape<DEC>::dec_of(warp) >= 0) {
     // ---------------- decoders: code words -> bf16 (w - sh), swizzled K-major ----------------
-    // Each thread owns two rows of every stage.  It copies their code words itself
+    // Each thread owns one row (two when there are two decoder warps) of every stage.  It
+    // copies their code words itself
     // (cp.async, kRawAhead stages ahead, into its own slots of a small ring: no other
     // thread touches them, so its own wait_group is the only synchronisation), keeps the
     // shift word of the current group and the one after it in registers, and fills the
     // decoded-weight ring, which the MMA warp frees stage by stage.
-    const int dt = tid - 32 * kFirstDec;  // rows dt + 32 kDecWarps h of the tile, h < kDecRows
+    const int dt = 32 * TcShape<DEC>::dec_of(warp) + lane;  // rows dt + 32 kDecWarps h, h < kDecRows
     const int wpr = p.mid / 8;
     const int wpg = p.group / 8;          // code words per group (group % 16 == 0)
     Cursor pre;                           // the stage whose code words are copied next
     pre.start(p, first_item);
     const auto issue_raw = [&](int slot) {
       if (pre.valid) {
-        const Item J = item_of(p, pre.it);
 #pragma unroll
         for (int h = 0; h < kDecRows; ++h) {
-          const int r = dt + 32 * kDecWarps * h, row = J.m0 + r;
+          const int r = dt + 32 * kDecWarps * h, row = pre.m0 + r;
           if (row < p.n0) {
-            const uint32_t* src = p.w + static_cast<int64_t>(row) * wpr + (J.st0 + pre.st) * (kBK / 8);
+            const uint32_t* src = p.w + static_cast<int64_t>(row) * wpr + (pre.st0 + pre.st) * (kBK / 8);
             cp_async16_tc(raw_of(slot) + 32u * r, src);
             cp_async16_tc(raw_of(slot) + 32u * r + 16u, src + 4);
           }
@@ -406,6 +451,9 @@ __global__ void __launch_bounds__(TcShape<DEC>::kThreads, 1) quant_dot_tc_kernel
         wcur[h] = row < p.n0 ? __ldg(sr + widx[h]) : 0u;
         wnxt[h] = (row < p.n0 && widx[h] + 1 < p.sw) ? __ldg(sr + widx[h] + 1) : 0u;
       }
+      // group of the stage's first code word and the words left in that group, advanced
+      // stage by stage
+      int g0 = gfirst, left0 = (gfirst + 1) * wpg - I.st0 * (kBK / 8);
       bool ok = true;
       for (int st = 0; st < I.nst; ++st, ++f) {
         issue_raw((f + kRawAhead) % kRawStages);
@@ -415,8 +463,6 @@ __global__ void __launch_bounds__(TcShape<DEC>::kThreads, 1) quant_dot_tc_kernel
           ok = false;
           break;
         }
-        const int w0 = (I.st0 + st) * (kBK / 8);  // first code word of the stage in the row
-        const int g0 = w0 / wpg, left0 = (g0 + 1) * wpg - w0;  // its group, words left in it
 #pragma unroll
         for (int h = 0; h < kDecRows; ++h) {
           const int r = dt + 32 * kDecWarps * h;
@@ -432,11 +478,29 @@ __global__ void __launch_bounds__(TcShape<DEC>::kThreads, 1) quant_dot_tc_kernel
             for (int c = 0; c < 8; ++c) cw[c] = 0u;
           }
           const uint32_t arow = a_of(as) + 128u * r;
-          int g = g0, left = left0;  // group of word c, and its words still to come
+          constexpr int NG = GW ? 8 / GW : 1;  // groups of the stage with fixed places
+          uint32_t addcs[NG];  // their bf16 pairs (-(128 + sh), -(128 + sh))
+          if constexpr (GW != 0) {
+            // the stage's NG groups g0 .. g0 + NG - 1 share one shift word (g0 is a
+            // multiple of NG), and the word advances by at most one a stage
+            if ((g0 >> 3) != widx[h]) {
+              widx[h] = g0 >> 3;
+              wcur[h] = wnxt[h];
+              wnxt[h] = (row < p.n0 && widx[h] + 1 < p.sw)
+                            ? __ldg(p.shifts + static_cast<int64_t>(row) * p.sw + widx[h] + 1)
+                            : 0u;
+            }
+#pragma unroll
+            for (int k = 0; k < NG; ++k)
+              addcs[k] = 0xC300C300u + 0x00010001u * ((wcur[h] >> (4 * ((g0 + k) & 7))) & 0xFu);
+          }
+          int g = g0, left = left0;  // GW = 0: group of word c, and its words still to come
           uint32_t addc = 0u;        // bf16 pair (-(128 + sh), -(128 + sh)) of group g
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
-            if (c == 0 || left == 0) {
+            if constexpr (GW != 0) {
+              addc = addcs[c / GW];
+            } else if (c == 0 || left == 0) {
               if (c != 0) {
                 ++g;
                 left = wpg;
@@ -451,7 +515,7 @@ __global__ void __launch_bounds__(TcShape<DEC>::kThreads, 1) quant_dot_tc_kernel
               const uint32_t sh = (wcur[h] >> (4 * (g & 7))) & 0xFu;
               addc = 0xC300C300u + 0x00010001u * sh;  // bf16 -(128 + sh): ulp 1 at 128
             }
-            --left;
+            if constexpr (GW == 0) --left;
             // even nibbles (elements 0, 2, 4, 6) in bytes 0..3 of t0, odd ones in t1; value
             // pair q is bytes q of t0 and t1 side by side, OR 0x4300 in each half is the
             // bf16 128 + nibble, and one bf16x2 add of -(128 + sh) leaves w - sh exactly
@@ -474,11 +538,16 @@ __global__ void __launch_bounds__(TcShape<DEC>::kThreads, 1) quant_dot_tc_kernel
           as = 0;
           aph ^= 1u;
         }
+        if constexpr (GW == 2 || GW == 4) {
+          g0 += 8 / GW;
+        } else {
+          for (left0 -= kBK / 8; left0 <= 0; left0 += wpg) ++g0;
+        }
       }
       if (!ok) break;
     }
     asm volatile("cp.async.wait_all;" ::: "memory");  // no copy of this thread is left in flight
-  } else {
+  } else if (warp >= kFirstEpi) {
     // ---------------- epilogue ----------------
     const int q = warp & 3;                 // tensor-memory lane quarter of this warp
     const int cq = (warp - kFirstEpi) >> 2; // its 64-column quarter of the tile
@@ -491,16 +560,17 @@ __global__ void __launch_bounds__(TcShape<DEC>::kThreads, 1) quant_dot_tc_kernel
       const Item I = item_of(p, it);
       const int row = I.m0 + r;
       const bool row_ok = row < p.n0;
-      float z[64];
+      uint64_t z2[32];  // the 64 outputs of this thread as fp32 pairs
 #pragma unroll
-      for (int i = 0; i < 64; ++i) z[i] = 0.0f;
+      for (int i = 0; i < 32; ++i) z2[i] = pk(0.0f, 0.0f);
       const int l_begin = I.st0 * kBK, l_end = l_begin + I.nst * kBK;
+      int g = l_begin / p.group, gb = (g + 1) * p.group;  // group of l, its end
       bool ok = true;
       for (int l = l_begin; l < l_end;) {
-        int nxt = min(l_end, (l / p.group + 1) * p.group);
+        int nxt = min(l_end, gb);
         if (p.group > kPieceCap) nxt = min(nxt, (l / kPieceCap + 1) * kPieceCap);
-        const int g = l / p.group;
         const float sc = row_ok ? __ldg(p.scales + static_cast<int64_t>(row) * p.ng + g) : 0.0f;
+        const uint64_t sc2 = pk(sc, sc);
         if (!__all_sync(kFull, tc_wait(smem_addr(&pfull_bar[buf]), (pf_bits >> buf) & 1u, &s_abort))) {
           ok = false;
           break;
@@ -509,17 +579,21 @@ __global__ void __launch_bounds__(TcShape<DEC>::kThreads, 1) quant_dot_tc_kernel
         tc_fence_after();
         const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(buf * kBN + 64 * cq);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float v[16];
-          tmem_ld16(ta + 16u * c, v);
+        for (int c = 0; c < 8; ++c) {  // z = fl32(sc * P + z) for each element, two per FMA
+          uint64_t v[4];
+          tmem_ld8_pairs(ta + 8u * c, v);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) z[16 * c + i] = __fmaf_rn(sc, v[i], z[16 * c + i]);
+          for (int i = 0; i < 4; ++i) z2[4 * c + i] = fma2(v[i], sc2, z2[4 * c + i]);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&pempty_bar[buf]));
         buf ^= 1;
         l = nxt;
+        if (l == gb) {
+          ++g;
+          gb += p.group;
+        }
       }
       if (!ok) break;
       if (row_ok) {
@@ -528,24 +602,23 @@ __global__ void __launch_bounds__(TcShape<DEC>::kThreads, 1) quant_dot_tc_kernel
         const int nv = min(64, p.n1 - c0);
         if (nv == 64 && zvec) {  // 16-byte stores (or reductions): 64 contiguous bytes a pair
 #pragma unroll
-          for (int i = 0; i < 64; i += 4) {
-            if (p.ksplit > 1)
-              asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(zr + i), "f"(z[i]),
-                           "f"(z[i + 1]), "f"(z[i + 2]), "f"(z[i + 3])
-                           : "memory");
-            else
-              asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(zr + i), "f"(z[i]), "f"(z[i + 1]),
-                           "f"(z[i + 2]), "f"(z[i + 3])
-                           : "memory");
+          for (int i = 0; i < 32; i += 2) {
+            if (p.ksplit > 1) red_pairs(zr + 2 * i, z2[i], z2[i + 1]);
+            else st_pairs(zr + 2 * i, z2[i], z2[i + 1]);
           }
-        } else if (p.ksplit > 1) {
-#pragma unroll
-          for (int i = 0; i < 64; ++i)
-            if (i < nv) atomicAdd(zr + i, z[i]);
         } else {
 #pragma unroll
-          for (int i = 0; i < 64; ++i)
-            if (i < nv) zr[i] = z[i];
+          for (int i = 0; i < 32; ++i) {
+            float z0, z1;
+            upk(z2[i], z0, z1);
+            if (p.ksplit > 1) {
+              if (2 * i < nv) atomicAdd(zr + 2 * i, z0);
+              if (2 * i + 1 < nv) atomicAdd(zr + 2 * i + 1, z1);
+            } else {
+              if (2 * i < nv) zr[2 * i] = z0;
+              if (2 * i + 1 < nv) zr[2 * i + 1] = z1;
+            }
+          }
         }
       }
     }
@@ -639,13 +712,17 @@ qz_status launch_quant_dot_tc(const uint32_t* w, const float* scales, const uint
   p.stages_total = static_cast<int>(stages_total);
   p.items = static_cast<int>(items);
   const bool four = group >= 128;
-  const void* kern = four ? reinterpret_cast<const void*>(&quant_dot_tc_kernel<4>)
-                          : reinterpret_cast<const void*>(&quant_dot_tc_kernel<2>);
-  if (!set_dyn_smem(kern, static_cast<int>(kSmemTc))) return QZ_ERR_CUDA;
+  const int gw = group % 64 == 0 ? 8 : group == 32 ? 4 : group == 16 ? 2 : 0;
+  void (*kern)(TcParams);
+  if (four) kern = gw == 8 ? &quant_dot_tc_kernel<4, 8> : &quant_dot_tc_kernel<4, 0>;
+  else if (gw == 8) kern = &quant_dot_tc_kernel<2, 8>;
+  else if (gw == 4) kern = &quant_dot_tc_kernel<2, 4>;
+  else if (gw == 2) kern = &quant_dot_tc_kernel<2, 2>;
+  else kern = &quant_dot_tc_kernel<2, 0>;
+  if (!set_dyn_smem(reinterpret_cast<const void*>(kern), static_cast<int>(kSmemTc))) return QZ_ERR_CUDA;
   if (ksplit > 1 && launch_zero_z(z, ld_z, n0, n1, s) != QZ_OK) return QZ_ERR_CUDA;
   const int grid = static_cast<int>(std::min<int64_t>(items, sms));
-  if (four) quant_dot_tc_kernel<4><<<grid, TcShape<4>::kThreads, kSmemTc, s>>>(p);
-  else quant_dot_tc_kernel<2><<<grid, TcShape<2>::kThreads, kSmemTc, s>>>(p);
+  kern<<<grid, four ? TcShape<4>::kThreads : TcShape<2>::kThreads, kSmemTc, s>>>(p);
   return launch_status();
 }
 
