@@ -332,13 +332,20 @@ __global__ void __launch_bounds__(TcShape<DEC>::kThreads, 1) quant_dot_tc_kernel
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issuer: lane 0 alone, the rest of the warp waits at the end ----
-    // An MMA is taken by the tensor core only when the one before it has started, so
-    // the loop keeps the instructions between two MMAs to a few adds: the piece
-    // boundaries come from a countdown of 16-wide steps and a running group boundary.
+    // An MMA is taken by the tensor core only when the one before it has started, so at
+    // most about two MMAs are queued while this thread works, and everything between two
+    // MMAs leaves the tensor core idle once those have run.  So the loop is software-
+    // pipelined: the next stage's "full" barriers are waited for before the stage's last
+    // MMA, and a stage's "empty" barriers are signalled after the next stage's first MMA
+    // (a commit tracks every MMA before it, so this frees the stage slightly later, which
+    // the ring depths absorb).  The piece boundaries come from a countdown of 16-wide
+    // steps and a running group boundary.
     if (lane == 0) {
-      int ys = 0, as = 0, buf = 0;
+      int ys = 0, as = 0, buf = 0, pys = 0, pas = 0;
       uint32_t yph = 0, aph = 0, pe_bits = 3u;  // bit b: parity of the next wait on "P empty" b
       bool issued = false;
+      bool ready = false;  // this stage's "full" barriers were waited for in the stage before
+      bool pend = false;   // stage (pys, pas) is read and its "empty" barriers not yet signalled
       for (int it = first_item; it < p.items && !s_abort; it += item_step) {
         const Item I = item_of(p, it);
         const uint32_t idesc = idesc_bf16(64 * I.nslab);
@@ -348,15 +355,33 @@ __global__ void __launch_bounds__(TcShape<DEC>::kThreads, 1) quant_dot_tc_kernel
         int left = 0;  // 16-wide steps of the open piece still to come (0: a new piece starts)
         bool open = false, acc = false, ok = true;
         for (int st = 0; st < I.nst && ok; ++st) {
-          if (!tc_wait(smem_addr(&yfull_bar[ys]), yph, &s_abort)) break;
-          if (!tc_wait(smem_addr(&afull_bar[as]), aph, &s_abort)) break;
+          if (!ready && (!tc_wait(smem_addr(&yfull_bar[ys]), yph, &s_abort) ||
+                         !tc_wait(smem_addr(&afull_bar[as]), aph, &s_abort)))
+            break;
+          ready = false;
           tc_fence_after();
           // A: rows of 128 bytes, 8-row groups 1 KiB apart, +32 bytes per 16 values of l;
           // B: 64-column boxes 8 KiB apart, 8-row groups of l 1 KiB apart, +2 KiB per 16 l
           const uint64_t ad0 = smem_desc_sw128(a_of(as), 16u, 1024u);
           const uint64_t bd0 = smem_desc_sw128(y_of(ys), kSlabBytes, 1024u);
+          const int ys1 = ys + 1 == kYStages ? 0 : ys + 1, as1 = as + 1 == kAStages ? 0 : as + 1;
+          const uint32_t yph1 = ys1 == 0 ? yph ^ 1u : yph, aph1 = as1 == 0 ? aph ^ 1u : aph;
+          const bool more = st + 1 < I.nst;  // the next stage belongs to this item
 #pragma unroll
           for (int j = 0; j < kBK / 16; ++j, l += 16) {
+            if (j == 1 && pend) {  // the stage before is read: free it in both rings
+              tc_commit(smem_addr(&yempty_bar[pys]));
+              tc_commit(smem_addr(&aempty_bar[pas]));
+              pend = false;
+            }
+            if (j == kBK / 16 - 1 && more) {  // the next stage, while two MMAs are queued
+              if (!tc_wait(smem_addr(&yfull_bar[ys1]), yph1, &s_abort) ||
+                  !tc_wait(smem_addr(&afull_bar[as1]), aph1, &s_abort)) {
+                ok = false;
+                break;
+              }
+              ready = true;
+            }
             if (left == 0) {  // a new piece: the end of its group (and of each 1024 values)
               if (open) {
                 tc_commit(smem_addr(&pfull_bar[buf]));
@@ -381,22 +406,23 @@ __global__ void __launch_bounds__(TcShape<DEC>::kThreads, 1) quant_dot_tc_kernel
             --left;
           }
           if (!ok) break;
-          tc_commit(smem_addr(&yempty_bar[ys]));  // both stages are free once these MMAs have read them
-          tc_commit(smem_addr(&aempty_bar[as]));
-          if (++ys == kYStages) {
-            ys = 0;
-            yph ^= 1u;
-          }
-          if (++as == kAStages) {
-            as = 0;
-            aph ^= 1u;
-          }
+          pend = true;  // both slots are free once these MMAs have read them
+          pys = ys;
+          pas = as;
+          ys = ys1;
+          yph = yph1;
+          as = as1;
+          aph = aph1;
         }
         if (s_abort || !ok) break;
         if (open) {
           tc_commit(smem_addr(&pfull_bar[buf]));
           buf ^= 1;
         }
+      }
+      if (pend && !s_abort) {
+        tc_commit(smem_addr(&yempty_bar[pys]));
+        tc_commit(smem_addr(&aempty_bar[pas]));
       }
       if (issued) {  // every MMA issued has completed before tensor memory is released
         tc_commit(smem_addr(&drain_bar));
@@ -518,7 +544,9 @@ __global__ void __launch_bounds__(TcShape<DEC>::kThreads, 1) quant_dot_tc_kernel
             if constexpr (GW == 0) --left;
             // even nibbles (elements 0, 2, 4, 6) in bytes 0..3 of t0, odd ones in t1; value
             // pair q is bytes q of t0 and t1 side by side, OR 0x4300 in each half is the
-            // bf16 128 + nibble, and one bf16x2 add of -(128 + sh) leaves w - sh exactly
+            // bf16 128 + nibble, and one bf16x2 add of -(128 + sh) leaves w - sh exactly.
+            // (Leaving the two byte masks to the OR below is one instruction less a word but
+            // made the four-decoder kernel spill more: 226 -> 249 us.)
             const uint32_t t0 = cw[c] & 0x0F0F0F0Fu, t1 = (cw[c] >> 4) & 0x0F0F0F0Fu;
             uint32_t v[4];
 #pragma unroll
