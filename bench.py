@@ -211,16 +211,11 @@ def compact_matrix(rows: list) -> dict:
     return out
 
 
-def measure_matrix(dev, peaks, flush, x4=None, reps=30, which=(1, 2, 3, 4, 5), max_rows=None) -> list:
-    import numpy as np
+def make_timed(dev, flush, reps):
+    """Mean CUDA-event time (ms) of fn on the current stream over `reps` launches after 3,
+    each after an L2 flush unless cold=False."""
     import torch
-    import precision_quantization_gb300 as qz
-    import workloads as W
-    out = []
     stream = torch.cuda.current_stream(dev)
-    sp = stream.cuda_stream
-    ws = qz.Workspace(dev)
-    st = torch.empty((qz.STATS_BYTES,), dtype=torch.uint8, device=dev)
 
     def timed(fn, cold=True):
         for _ in range(3):
@@ -240,6 +235,36 @@ def measure_matrix(dev, peaks, flush, x4=None, reps=30, which=(1, 2, 3, 4, 5), m
         # 5-50 us launches of the smaller workloads, and the mean over many launches with
         # varying start phases is not biased by the step the way a median is
         return statistics.mean(ts)
+    return timed
+
+
+# Quantized products on the tensor cores beyond the matrix rows: square and prefill-sized
+# shapes, the group sizes with their own decode forms, and a short activation block.
+QDOT_SWEEP = [(4096, 4096, 128, 4096), (8192, 8192, 128, 4096), (32768, 8192, 128, 2048),
+              (4096, 4096, 64, 4096), (4096, 4096, 32, 4096), (4096, 4096, 128, 512)]
+
+
+def measure_qdot_sweep(dev, peaks, flush, reps=30) -> list:
+    timed = make_timed(dev, flush, reps)
+    out = []
+    for n0, mid, group, n1 in QDOT_SWEEP:
+        row = measure_qdot(f"weight-{n0}x{mid}", n0, mid, group, n1, timed, peaks, dev)
+        out.append({k: row[k] for k in ("workload", "granularity", "dequantize_us", "tflops",
+                                        "tflops_peak", "tflops_frac")})
+    return out
+
+
+def measure_matrix(dev, peaks, flush, x4=None, reps=30, which=(1, 2, 3, 4, 5), max_rows=None) -> list:
+    import numpy as np
+    import torch
+    import precision_quantization_gb300 as qz
+    import workloads as W
+    out = []
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    ws = qz.Workspace(dev)
+    st = torch.empty((qz.STATS_BYTES,), dtype=torch.uint8, device=dev)
+    timed = make_timed(dev, flush, reps)
 
     for k, rows, runs in MATRIX:
         if k not in which:
@@ -554,6 +579,8 @@ def main():
                     help="print only the per-format matrix (one JSON line)")
     ap.add_argument("--matrix-workloads", default="1,2,3,4,5",
                     help="comma-separated workload numbers of the matrix")
+    ap.add_argument("--qdot-sweep", action="store_true",
+                    help="print only the quantized-product sweep (one JSON line, TFLOP/s)")
     ap.add_argument("--matrix-rows", type=int, default=None,
                     help="at most this many rows of each matrix workload (small cases for profiling)")
     ap.add_argument("--rows", type=int, default=ROWS,
@@ -574,6 +601,12 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     which = tuple(int(v) for v in args.matrix_workloads.split(",") if v)
+    if args.qdot_sweep:
+        flush = L2Flush(dev)
+        m = measure_qdot_sweep(dev, measured_peaks(), flush)
+        print(json.dumps({"metric": "quantized product TFLOP/s (bf16 tensor cores)", "unit": "TFLOP/s",
+                          "products": m}), flush=True)
+        return
     if args.matrix_only:
         flush = L2Flush(dev)
         m = measure_matrix(dev, measured_peaks(), flush, which=which, max_rows=args.matrix_rows)
