@@ -22,21 +22,22 @@
 //   warp 1        lane 0 issues the MMAs: four 128 x N x 16 steps per stage into one of two
 //                 tensor-memory buffers of 256 fp32 columns, a new buffer at every group
 //                 boundary (and every 1024 values of a longer group), commits each stage's
-//                 completion to the "empty" barriers of both rings and each finished group
-//                 to "P full".
-//   warps 2-5     decode (warps 2-3 when groups are shorter than 128): each thread takes one
-//                 (two) weight rows; it copies their code words
-//                 itself (cp.async, kRawAhead stages ahead), turns every word into eight
-//                 bf16 values w - sh (nibbles split by mask, paired by a byte permute,
-//                 OR-ed into bf16 128 + w, one bf16x2 add of -(128 + sh)) and stores them
-//                 in a ring of kAStages stages in the MMA's K-major 128-byte swizzled
-//                 layout, then signals "A full".  The decoders run ahead of the MMAs
-//                 independently of the activation copies, so the MMA warp's loop waits on
-//                 the TMA ring alone.
-//   warps 6-21    epilogue (4-19): warp w reads tensor-memory lanes 32 (w % 4) .. + 31 (its rows)
-//                 and 64 of the 256 columns; for every finished group it adds sc * P into
-//                 64 fp32 registers, frees the buffer, and at the end of the item stores z
-//                 (16-byte stores, or reductions when the item is one slice of several).
+//                 completion to the "empty" barriers of both rings (after the next stage's
+//                 first MMA) and each finished group to "P full".
+//   decoders      warps 2, 3, 4 and 6 (groups of 128 and more; one weight row per thread)
+//                 or warps 2 and 3 (shorter groups; two rows per thread), never a warp on
+//                 the MMA warp's scheduler (w % 4 == 1).  Each thread copies its rows'
+//                 code words itself (cp.async, kRawAhead stages ahead), turns every word
+//                 into eight bf16 values w - sh (nibbles split by mask, paired by a byte
+//                 permute, OR-ed into bf16 128 + w, one bf16x2 add of -(128 + sh)) and
+//                 stores them in a ring of kAStages stages in the MMA's K-major 128-byte
+//                 swizzled layout, then signals "A full".  The decoders run ahead of the
+//                 MMAs independently of the activation copies.
+//   epilogue      the 16 warps after them (8-23, or 4-19): warp w reads tensor-memory lanes
+//                 32 (w % 4) .. + 31 (its rows) and 64 of the 256 columns; for every
+//                 finished group it adds sc * P into its 64 fp32 outputs (packed FMAs),
+//                 frees the buffer, and at the end of the item stores z (16-byte stores, or
+//                 reductions when the item is one slice of several).
 #include <cuda.h>  // CUtensorMap and its enumerators (types only; the encoder is looked up)
 #include <cudaTypedefs.h>
 
@@ -239,10 +240,11 @@ struct Cursor {
   }
 };
 
-// DEC decoder warps: four keep pace with the MMAs for groups of 128 and more (4096^3 at
-// group 128: 345 -> 296 us); with their 704 threads the epilogue's 64 accumulators spill a
-// little, which costs more than the extra decoders gain when every 16 to 64 values end a
-// group (group 32: 467 -> 715 us, group 64: 392 -> 407 us), so those run with two.
+// DEC decoder warps: four for groups of 128 and more (measured when introduced, 4096^3 at
+// group 128: 345 -> 296 us); with their 768 threads (80 registers each) the epilogue's 64
+// accumulators spill a little, which costs more than the extra decoders gain when every
+// 16 to 64 values end a group (then: group 32 467 -> 715 us, group 64 392 -> 407 us), so
+// those run with two (640 threads, 96 registers).
 //
 // GW: code words per group when a stage's groups sit at fixed places in it -- 8 for every
 // group that is a multiple of 64 values (a stage lies inside one group), 4 for groups of
@@ -435,11 +437,10 @@ __global__ void __launch_bounds__(TcShape<DEC>::kThreads, 1) quant_dot_tc_kernel
   } else if (warp < kFirstEpi && TcShape<DEC>::dec_of(warp) >= 0) {
     // ---------------- decoders: code words -> bf16 (w - sh), swizzled K-major ----------------
     // Each thread owns one row (two when there are two decoder warps) of every stage.  It
-    // copies their code words itself
-    // (cp.async, kRawAhead stages ahead, into its own slots of a small ring: no other
-    // thread touches them, so its own wait_group is the only synchronisation), keeps the
-    // shift word of the current group and the one after it in registers, and fills the
-    // decoded-weight ring, which the MMA warp frees stage by stage.
+    // copies their code words itself (cp.async, kRawAhead stages ahead, into its own slots
+    // of a small ring: no other thread touches them, so its own wait_group is the only
+    // synchronisation), keeps the shift word of the current group and the one after it in
+    // registers, and fills the decoded-weight ring, which the MMA warp frees stage by stage.
     const int dt = 32 * TcShape<DEC>::dec_of(warp) + lane;  // rows dt + 32 kDecWarps h, h < kDecRows
     const int wpr = p.mid / 8;
     const int wpg = p.group / 8;          // code words per group (group % 16 == 0)
