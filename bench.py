@@ -722,7 +722,7 @@ def main():
             t1 = time.perf_counter()
             plan.run(xh)
             e_ms.append((time.perf_counter() - t1) * 1e3)
-        if plan.ws.status() != 0:
+        if plan.status() != 0:
             raise RuntimeError("e2e: device status flags raised")
         for j, f in enumerate((qz.QZ_MXFP4, qz.QZ_NVFP4)):  # same statistics as the kernel step
             a, b = plan.read_stats(j), stats_host[f]
@@ -737,7 +737,8 @@ def main():
                "ms_per_step": round(em, 3), "ms_mean": round(statistics.mean(e_ms), 3),
                "steps": len(e_ms), "timing": "host clock per round trip, median",
                "chunk_rows": args.e2e_chunk_rows,
-               "api": "streamed.HostRoundTrip.run (pinned host in/out, copies overlapped)"}
+               "api": "qz_host_run, one C-ABI call per round trip (pinned host in/out, "
+                      "copies overlapped with the kernels on the library's own streams)"}
 
     matrix = None
     if not args.no_matrix and rank == 0:

@@ -61,7 +61,8 @@
  * cols % block_size == 0.
  *
  * Ownership and concurrency.  The caller allocates every buffer (all device memory except
- * the host pointer of qz_get_device_status).  The library allocates nothing; its only
+ * the host pointer of qz_get_device_status).  The library allocates nothing, except a host
+ * round-trip plan (qz_host_plan_create, at the end of this header); its only other
  * host-side state is a per-device cache of launch parameters (SM count, resident CTAs per
  * SM, shared-memory opt-ins), guarded by a mutex.  Every call is asynchronous on `stream`
  * (NULL = the legacy default stream); argument errors are returned synchronously, before
@@ -308,6 +309,76 @@ QZ_API qz_status qz_selftest_pipeline_timeout(void* ws, uint64_t limit_ns, qz_st
 /* Synchronize `stream`, then copy the workspace status word (QZ_FLAG_* bits, sticky until
  * qz_workspace_init) into *flags_host. */
 QZ_API qz_status qz_get_device_status(const void* ws, uint32_t* flags_host, qz_stream_t stream);
+
+/* ---- Host round trip ---------------------------------------------------------------------
+ * The quantization of a tensor that sits in host memory: x goes to the device in chunks of
+ * whole rows, each chunk is quantized (with the fused statistics when the plan asks for
+ * them) and dequantized as soon as it has landed, and its codes and scales go back while
+ * later chunks arrive -- three CUDA streams of the plan's own (host-to-device, kernels,
+ * device-to-host), ordered by events.  Formats with a per-tensor scale (TENSOR, NVFP4
+ * BLOCK) take the amax of every chunk as it lands and are quantized once the last chunk is
+ * in, with the tensor's amax (the largest of the chunk amaxes) supplied.  The operations
+ * are the ones of qz_quantize / qz_dequantize / qz_stats_merge above, which the plan calls:
+ * codes, scales and tensor scales are bit-identical to one qz_quantize of the whole tensor
+ * (blocks and rows never straddle a chunk), the statistics are the chunks' merged.  The
+ * post has no counterpart: this is the runtime around the calls above.
+ *
+ * Unlike the other calls, a plan allocates, once, at qz_host_plan_create on the current
+ * device: a device copy of x ([rows, cols]), a workspace, per-chunk statistics and amaxes,
+ * three streams and their events; qz_host_plan_destroy frees them.  qz_host_run allocates
+ * nothing.  A plan is used by one host thread at a time. */
+#define QZ_HOST_MAX_RUNS 16
+
+typedef struct qz_host_plan qz_host_plan;
+
+/* Buffers of one run (one format / granularity) of a plan.  Device outputs as qz_quantize /
+ * qz_dequantize write them for the whole tensor (caller-allocated, dense):
+ *   codes, scales (NULL when the format has none), tensor_scale (one fp32, required),
+ *   y     the dequantized tensor, [rows, cols] of the plan's out_dtype, or NULL for none,
+ *   stats the merged statistics (required when the plan fuses them, else ignored).
+ * Host copies, each NULL for "not copied": codes_host, scales_host (the same bytes as the
+ * device buffers), tensor_scale_host (one fp32), stats_host (one qz_stats).  Host memory
+ * that is page-locked (cudaHostAlloc / cudaHostRegister) lets the copies overlap the
+ * kernels; pageable memory works, with copies that do not overlap. */
+typedef struct {
+  void* codes;
+  void* scales;
+  float* tensor_scale;
+  void* y;
+  qz_stats* stats;
+  void* codes_host;
+  void* scales_host;
+  float* tensor_scale_host;
+  qz_stats* stats_host;
+} qz_host_io;
+
+/* A plan for `n_runs` (1 .. QZ_HOST_MAX_RUNS) quantizations of one [rows, cols] tensor:
+ * runs[j] is a descriptor as for qz_quantize; every run has the same in_dtype, rows and cols,
+ * and ld == cols (the host tensor is dense).  chunk_rows >= 1 rows go over per copy (a
+ * chunk larger than the tensor is the whole tensor).  out_dtype (QZ_BF16 / QZ_F32) is the
+ * dtype of the dequantized tensors; fuse_stats != 0 fuses the error statistics.
+ * Errors: QZ_ERR_NULL (runs or plan NULL), QZ_ERR_SHAPE (n_runs or chunk_rows out of range,
+ * runs of different shapes, ld != cols), QZ_ERR_ENUM (out_dtype, mixed in_dtype), every
+ * descriptor error of qz_quantize, QZ_ERR_CUDA (an allocation failed; nothing is kept).
+ * *plan is NULL on every error. */
+QZ_API qz_status qz_host_plan_create(const qz_desc* runs, int32_t n_runs, int64_t chunk_rows,
+                                     int32_t out_dtype, int32_t fuse_stats, qz_host_plan** plan);
+
+/* One round trip of x_host (host, [rows, cols] dense, the plan's in_dtype; may be NULL for
+ * an empty tensor): io[j] holds the buffers of run j (n_runs entries).  Returns when every
+ * device output and host copy is complete (the plan's streams are synchronised; the
+ * caller's streams are not touched).  Errors: QZ_ERR_NULL (plan, io, x_host, or a required
+ * buffer of io NULL -- checked before anything is enqueued), a status of one of the calls
+ * above (enqueueing stops there; what was enqueued is waited for), QZ_ERR_CUDA (a copy or
+ * event failed). */
+QZ_API qz_status qz_host_run(qz_host_plan* plan, const void* x_host, const qz_host_io* io);
+
+/* Status word of the plan's workspace (QZ_FLAG_* bits raised by its calls, sticky), into
+ * *flags_host; synchronous. */
+QZ_API qz_status qz_host_plan_status(const qz_host_plan* plan, uint32_t* flags_host);
+
+/* Wait for the plan's streams and free everything it allocated.  NULL is ignored. */
+QZ_API void qz_host_plan_destroy(qz_host_plan* plan);
 
 #ifdef __cplusplus
 }

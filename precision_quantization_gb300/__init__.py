@@ -40,7 +40,9 @@ BLOCK_SIZE = {QZ_MXFP4: 32, QZ_NVFP4: 16, QZ_INT4: 32}  # INT4: the default grou
 ABI_SYMBOLS = ("qz_status_string", "qz_workspace_size", "qz_workspace_init", "qz_amax",
                "qz_quantize", "qz_quantize_delayed", "qz_dequantize", "qz_error_stats",
                "qz_error_stats_noalloc", "qz_error_stats_noalloc_status", "qz_stats_merge", "qz_dequantize_asym4", "qz_quant_dot",
-               "qz_selftest_pipeline_timeout", "qz_get_device_status")
+               "qz_selftest_pipeline_timeout", "qz_get_device_status", "qz_host_plan_create",
+               "qz_host_run", "qz_host_plan_status", "qz_host_plan_destroy")
+QZ_HOST_MAX_RUNS = 16
 
 
 class QzDesc(C.Structure):
@@ -56,6 +58,14 @@ class QzStats(C.Structure):
 
 
 STATS_BYTES = C.sizeof(QzStats)
+
+
+class QzHostIo(C.Structure):
+    """qz_host_io: one run's device outputs and host copies (0 / None = absent)."""
+    _fields_ = [("codes", C.c_void_p), ("scales", C.c_void_p), ("tensor_scale", C.c_void_p),
+                ("y", C.c_void_p), ("stats", C.c_void_p), ("codes_host", C.c_void_p),
+                ("scales_host", C.c_void_p), ("tensor_scale_host", C.c_void_p),
+                ("stats_host", C.c_void_p)]
 
 
 class QzError(RuntimeError):
@@ -93,6 +103,10 @@ def lib():
             "qz_selftest_pipeline_timeout": (i32, [vp, C.c_uint64, vp]),
             "qz_quant_dot": (i32, [vp, vp, vp, C.c_int64, C.c_int64, C.c_int64, vp, C.c_int64,
                                    C.c_int64, vp, C.c_int64, vp]),
+            "qz_host_plan_create": (i32, [dp, i32, C.c_int64, i32, i32, C.POINTER(vp)]),
+            "qz_host_run": (i32, [vp, vp, C.POINTER(QzHostIo)]),
+            "qz_host_plan_status": (i32, [vp, C.POINTER(C.c_uint32)]),
+            "qz_host_plan_destroy": (None, [vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -136,6 +150,31 @@ def qz_dequantize_asym4(w: int, scales: int, shifts: int, rows: int, cols: int, 
                         y: int, ld: int, out_dtype: int, stream: int = 0) -> int:
     return lib().qz_dequantize_asym4(w, scales, shifts, rows, cols, group, y, ld, out_dtype,
                                      stream)
+
+
+def qz_host_plan_create(runs, chunk_rows: int, out_dtype: int, fuse_stats: bool):
+    """runs: sequence of QzDesc.  Returns (status, plan handle or None)."""
+    arr = (QzDesc * len(runs))(*runs) if len(runs) else None
+    h = C.c_void_p()
+    st = lib().qz_host_plan_create(arr, len(runs), chunk_rows, out_dtype, int(bool(fuse_stats)),
+                                   C.byref(h))
+    return st, (h.value if st == QZ_OK else None)
+
+
+def qz_host_run(plan: int, x_host: int | None, io) -> int:
+    """io: sequence of QzHostIo, one per run of the plan."""
+    arr = (QzHostIo * len(io))(*io)
+    return lib().qz_host_run(plan, x_host, arr)
+
+
+def qz_host_plan_status(plan: int):
+    flags = C.c_uint32(0)
+    st = lib().qz_host_plan_status(plan, C.byref(flags))
+    return st, flags.value
+
+
+def qz_host_plan_destroy(plan: int | None) -> None:
+    lib().qz_host_plan_destroy(plan)
 
 
 def qz_quant_dot(w: int, scales: int, shifts: int, n0: int, mid: int, group: int, y: int,

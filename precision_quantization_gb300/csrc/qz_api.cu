@@ -182,6 +182,12 @@ qz_status check_ws(const void* ws) {
 }
 
 }  // namespace
+
+qz_status validate_desc(const qz_desc* d) {
+  const qz_status st = check_desc(d);
+  return st != QZ_OK ? st : check_dtype(d->in_dtype);
+}
+
 }  // namespace qz
 
 using namespace qz;

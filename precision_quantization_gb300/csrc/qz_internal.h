@@ -81,4 +81,7 @@ inline qz_status launch_status() {
   return cudaGetLastError() == cudaSuccess ? QZ_OK : QZ_ERR_CUDA;
 }
 
+// The descriptor checks of qz_quantize (fields, shape, input dtype), without a launch.
+qz_status validate_desc(const qz_desc* d);
+
 }  // namespace qz

@@ -204,3 +204,49 @@ def test_binding_fails_loudly_without_library(qz, monkeypatch, tmp_path):
     monkeypatch.setattr(mod, "_lib", None)
     with pytest.raises(ImportError):
         mod.lib()
+
+
+def test_host_io_layout_matches_header(qz, tmp_path):
+    src = tmp_path / "hostio.c"
+    src.write_text(
+        '#include <stdio.h>\n#include <stddef.h>\n#include "qz.h"\n'
+        "int main(void){printf(\"%zu %zu %zu %zu %zu %d\\n\", sizeof(qz_host_io),"
+        " offsetof(qz_host_io, y), offsetof(qz_host_io, stats), offsetof(qz_host_io, codes_host),"
+        " offsetof(qz_host_io, stats_host), QZ_HOST_MAX_RUNS); return 0;}\n")
+    exe = tmp_path / "hostio"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)],
+                   check=True)
+    got = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    io = qz.QzHostIo
+    assert got == [C.sizeof(io), io.y.offset, io.stats.offset, io.codes_host.offset,
+                   io.stats_host.offset, qz.QZ_HOST_MAX_RUNS]
+
+
+def test_host_plan_argument_errors(qz):
+    """Every argument error of qz_host_plan_create comes back before a CUDA call, with the
+    plan handle left NULL; the other host-plan calls reject a NULL plan."""
+    d = qz.make_desc("nvfp4", qz.QZ_BF16, "block", 64, 256)
+    e = qz.make_desc("e4m3", qz.QZ_BF16, "tensor", 64, 256)
+    create = qz.qz_host_plan_create
+    assert create([d, e], 0, qz.QZ_BF16, True) == (qz.QZ_ERR_SHAPE, None)   # chunk_rows
+    assert create([], 16, qz.QZ_BF16, True) == (qz.QZ_ERR_NULL, None)       # no runs
+    assert create([d] * 17, 16, qz.QZ_BF16, True) == (qz.QZ_ERR_SHAPE, None)
+    assert create([d], 16, 9, True) == (qz.QZ_ERR_ENUM, None)               # out dtype
+    mixed = qz.make_desc("e4m3", qz.QZ_F32, "tensor", 64, 256)
+    assert create([d, mixed], 16, qz.QZ_BF16, True) == (qz.QZ_ERR_ENUM, None)
+    other_rows = qz.make_desc("e4m3", qz.QZ_BF16, "tensor", 65, 256)
+    assert create([d, other_rows], 16, qz.QZ_BF16, True) == (qz.QZ_ERR_SHAPE, None)
+    strided = qz.make_desc("nvfp4", qz.QZ_BF16, "block", 64, 256, 512)
+    assert create([strided], 16, qz.QZ_BF16, True) == (qz.QZ_ERR_SHAPE, None)
+    bad_fmt = qz.make_desc("nvfp4", qz.QZ_BF16, "block", 64, 256)
+    bad_fmt.format = 9
+    assert create([bad_fmt], 16, qz.QZ_BF16, True) == (qz.QZ_ERR_ENUM, None)
+    ragged = qz.make_desc("e4m3", qz.QZ_BF16, "tensor", 64, 40)
+    ragged_nv = qz.make_desc("nvfp4", qz.QZ_BF16, "block", 64, 48)
+    ragged_nv.cols, ragged_nv.ld = 40, 40
+    assert create([ragged, ragged_nv], 16, qz.QZ_BF16, True) == (qz.QZ_ERR_SHAPE, None)
+    assert qz.lib().qz_host_plan_create(None, 1, 16, qz.QZ_BF16, 1, None) == qz.QZ_ERR_NULL
+    assert qz.qz_host_run(None, FAKE, [qz.QzHostIo()]) == qz.QZ_ERR_NULL
+    assert qz.qz_host_plan_status(None)[0] == qz.QZ_ERR_NULL
+    qz.qz_host_plan_destroy(None)  # a no-op

@@ -54,7 +54,7 @@ def test_round_trip_lognormal_chunks(chunk_rows):
     plan.run(host_tensor(x_np))
     for j, (f, g) in enumerate(RUNS):
         check_run(plan, j, x_np, f, g)
-    assert plan.ws.status() == 0
+    assert plan.status() == 0
 
 
 def test_round_trip_reused_plan_f32_edge_mix():
@@ -90,6 +90,42 @@ def test_round_trip_without_stats():
         assert np.array_equal(to_host_bits(plan.y[j]), o["y"]["bf16"]), (f, g)
     assert plan.bytes_out() == sum(t.numel() * t.element_size() for h in plan.host
                                    for k, t in h.items() if t is not None and k != "stats")
+
+
+def test_round_trip_pageable_input():
+    """A host tensor that is not page-locked: the copies do not overlap, the results are
+    the same."""
+    from precision_quantization_gb300.streamed import HostRoundTrip
+    torch = torch_mod()
+    rows, cols = 257, 512
+    x_np = W.lognormal_signed(rows, cols, seed=43)
+    xh = torch.from_numpy(np.ascontiguousarray(x_np).view(np.int16)).view(torch.bfloat16)
+    assert not xh.is_pinned()
+    plan = HostRoundTrip(rows, cols, RUNS, chunk_rows=100)
+    plan.run(xh)
+    for j, (f, g) in enumerate(RUNS):
+        check_run(plan, j, x_np, f, g)
+
+
+def test_host_run_missing_buffer():
+    """A required device buffer missing from one run's io: QZ_ERR_NULL before anything is
+    enqueued, and the plan still works afterwards."""
+    import precision_quantization_gb300 as qz
+    from precision_quantization_gb300.streamed import HostRoundTrip
+    rows, cols = 64, 256
+    x_np = W.activation_like(rows, cols, seed=44)
+    plan = HostRoundTrip(rows, cols, RUNS, chunk_rows=32)
+    xh = host_tensor(x_np)
+    for field in ("codes", "scales", "tensor_scale", "stats"):
+        io = [qz.QzHostIo.from_buffer_copy(v) for v in plan.io]
+        j = 0 if field == "scales" else 2  # MXFP4 has scales; E4M3 TENSOR has none
+        setattr(io[j], field, None)
+        assert qz.qz_host_run(plan.plan, xh.data_ptr(), io) == qz.QZ_ERR_NULL, field
+    assert qz.qz_host_run(plan.plan, None, plan.io) == qz.QZ_ERR_NULL  # x_host
+    plan.run(xh)
+    for j, (f, g) in enumerate(RUNS):
+        check_run(plan, j, x_np, f, g)
+    assert plan.status() == 0
 
 
 def test_round_trip_empty():
