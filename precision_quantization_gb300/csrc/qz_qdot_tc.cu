@@ -453,8 +453,10 @@ __global__ void __launch_bounds__(TcShape<DEC>::kThreads, 1) quant_dot_tc_kernel
           const int r = dt + 32 * kDecWarps * h, row = pre.m0 + r;
           if (row < p.n0) {
             const uint32_t* src = p.w + static_cast<int64_t>(row) * wpr + (pre.st0 + pre.st) * (kBK / 8);
-            cp_async16_tc(raw_of(slot) + 32u * r, src);
-            cp_async16_tc(raw_of(slot) + 32u * r + 16u, src + 4);
+            // the first 16 bytes of every row, then the second 16: a warp's 16-byte loads
+            // below are then consecutive (a row-major 32-byte stride is a 2-way conflict)
+            cp_async16_tc(raw_of(slot) + 16u * r, src);
+            cp_async16_tc(raw_of(slot) + 16u * (kBM + r), src + 4);
           }
         }
         pre.next(p, item_step);
@@ -496,8 +498,8 @@ __global__ void __launch_bounds__(TcShape<DEC>::kThreads, 1) quant_dot_tc_kernel
           const int row = I.m0 + r;
           uint32_t cw[8];
           if (row < p.n0) {
-            const uint4 c0 = lds128_tc(raw + 32u * r);
-            const uint4 c1 = lds128_tc(raw + 32u * r + 16u);
+            const uint4 c0 = lds128_tc(raw + 16u * r);
+            const uint4 c1 = lds128_tc(raw + 16u * (kBM + r));
             cw[0] = c0.x; cw[1] = c0.y; cw[2] = c0.z; cw[3] = c0.w;
             cw[4] = c1.x; cw[5] = c1.y; cw[6] = c1.z; cw[7] = c1.w;
           } else {
