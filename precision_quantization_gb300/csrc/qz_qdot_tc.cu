@@ -384,7 +384,11 @@ __global__ void __launch_bounds__(TcShape<DEC>::kThreads, 1) quant_dot_tc_kernel
               }
               ready = true;
             }
-            if (left == 0) {  // a new piece: the end of its group (and of each 1024 values)
+            // where a piece can start: groups that are multiples of 64 values begin at a
+            // stage, groups of 32 at every other 16-wide step, groups of 16 at every step;
+            // other groups anywhere.  Only those places carry the piece code.
+            const bool may_start = GW == 0 || GW == 2 || (GW == 4 && (j & 1) == 0) || (GW == 8 && j == 0);
+            if (may_start && left == 0) {  // a new piece: the end of its group (and of each 1024 values)
               if (open) {
                 tc_commit(smem_addr(&pfull_bar[buf]));
                 buf ^= 1;
