@@ -468,7 +468,22 @@ __global__ void __launch_bounds__(kThreads, PipeShape<FMT>::kCtas) quant4_pipe_k
     const uint32_t stage = P.stage(k);
     // MXFP4: two chunks in flight per thread (measured 127.6 -> 125.6 us with statistics on
     // a 32768 x 8192 bf16 tensor); NVFP4: one, which keeps its larger chunk code from
-    // running out of registers (148 -> 154 us when unrolled by two)
+    // running out of registers (148 -> 154 us when unrolled by two).
+    // A tile wholly inside the tensor takes a loop in which every chunk is valid: no bounds
+    // test, zero fill or guarded store per chunk (NVFP4 with statistics 148 -> 146 us).
+    if ((tile + 1) * kTileChunks <= n_chunks) {
+#pragma unroll(PipeShape<FMT>::kUnroll)
+      for (int c = 0; c < kCPT; ++c) {
+        const int j = c * kThreads + tid;
+        const int64_t u = tile * kTileChunks + j;
+        uint32_t w[8];
+        lds32B(w, stage + 32u * j);
+        if (!STATS || acc.T >= 1.0f)
+          q4_chunk<FMT, DT, UNIT, STATS, SR, false, AMAX>(a, cx, w, u, true, lane, acc, tpart, am);
+        else
+          q4_chunk<FMT, DT, UNIT, STATS, SR, true, AMAX>(a, cx, w, u, true, lane, acc, tpart, am);
+      }
+    } else
 #pragma unroll(PipeShape<FMT>::kUnroll)
     for (int c = 0; c < kCPT; ++c) {
       const int j = c * kThreads + tid;
