@@ -742,6 +742,123 @@ __global__ void __launch_bounds__(kThreads) quant8_rowslot_kernel(Q8Args a, floa
   stats_finish(acc, a.ws, a.stats, static_cast<uint64_t>(g.rows * g.cols));
 }
 
+// Per-row scale with the fused statistics, rows of whole 32-byte chunks whose chunk count is
+// a multiple of 4 (at most kRowQuadMaxBytes): a group of four warps per row, each warp a
+// quarter of it.  Each warp owns two shared-memory slots of a quarter row: lane 0 copies its
+// quarter of the group's next row into one (a bulk copy on the warp's own barrier) while the
+// warp works on the other, so the copies overlap the arithmetic.  The quarter amaxes meet in
+// shared memory behind a named barrier of the group's 128 threads; then each warp quantizes
+// its quarter with the statistics.  Rows are dealt to groups in turn, so the work is even to
+// a quarter of a row per warp (with a warp per row, 4096 rows on 3648 warps left a second,
+// nearly empty round paying a whole row's latency).  Every warp of a group takes the same
+// rows and reaches every barrier, whatever its copies do.
+constexpr int kQuadWarps = 4;
+constexpr int kRowQuadMaxBytes = 48 * 1024;
+
+template <int FMT, int DT>
+__global__ void __launch_bounds__(kThreads, 3) quant8_rowquad_kernel(Q8Args a, float zero, uint32_t slot_bytes) {
+  constexpr int EPC = Elem<DT>::kPer32B;
+  constexpr int kGroups = kWarps / kQuadWarps;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t bars[kWarps][2];
+  __shared__ float s_am[2][kWarps];  // quarter amaxes, by the parity of the row iteration
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int grp = warp / kQuadWarps, q = warp % kQuadWarps;
+  const Geom& g = a.g;
+  const int cpq = static_cast<int>(g.cpr) / kQuadWarps;  // chunks per quarter
+  const uint32_t qbytes = static_cast<uint32_t>(cpq) * 32u;
+  if (a.tscale_out && blockIdx.x == 0 && tid == 0) *a.tscale_out = 1.0f;
+  const uint32_t slots = smem_addr(smem) + static_cast<uint32_t>(warp) * 2u * slot_bytes;
+  const uint32_t bar0 = smem_addr(&bars[warp][0]), bar1 = smem_addr(&bars[warp][1]);
+  if (lane == 0) {
+    mbar_init(bar0, 1);
+    mbar_init(bar1, 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
+  const int64_t step = static_cast<int64_t>(gridDim.x) * kGroups;
+  const int64_t first = static_cast<int64_t>(blockIdx.x) * kGroups + grp;
+  const char* xq = static_cast<const char*>(a.x) + static_cast<int64_t>(q) * cpq * 32;
+  const auto issue = [&](int64_t row, int b) {  // lane 0: this warp's quarter of `row` into slot b
+    const uint32_t bar = b ? bar1 : bar0;
+    mbar_expect_tx(bar, qbytes);
+    bulk_g2s(slots + static_cast<uint32_t>(b) * slot_bytes, xq + row * g.ld * Elem<DT>::kBytes, qbytes, bar);
+  };
+  if (lane == 0 && first < g.rows) issue(first, 0);
+  const uint64_t z2 = pk(zero, zero);
+  StatAcc acc;
+  uint32_t am_unused = 0u, phase = 0u;  // bit b: parity of the next wait on slot b
+  int k = 0;
+  for (int64_t row = first; row < g.rows; row += step, ++k) {  // the same rows for the whole group
+    const int b = k & 1;
+    if (lane == 0 && row + step < g.rows) issue(row + step, b ^ 1);  // slot b ^ 1: read in iteration k - 1
+    const uint32_t bar = b ? bar1 : bar0;
+    if (!__all_sync(kFull, mbar_wait(bar, (phase >> b) & 1u, kWaitLimitNs))) {
+      // the copy did not land within the limit: flag it and let it land (bounded); the warp
+      // goes on with whatever the slot holds, so that the group's barriers stay matched
+      if (lane == 0) {
+        flag_status(a.ws, QZ_FLAG_PIPELINE_TIMEOUT);
+        mbar_wait(bar, (phase >> b) & 1u, kWaitLimitNs);
+      }
+      __syncwarp();
+    }
+    phase ^= 1u << b;
+    const uint32_t slot = slots + static_cast<uint32_t>(b) * slot_bytes;
+    // pass 1: the quarter's amax (NaN propagates), then the row's from the group
+    float A = 0.0f;
+#pragma unroll 1
+    for (int j = lane; j < cpq; j += 32) {
+      uint32_t w[8];
+      lds32B(w, slot + 32u * static_cast<uint32_t>(j));
+      if constexpr (DT == QZ_BF16) {
+        A = absmax_nan(A, bf16x16_absmax(w));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) A = absmax3(A, __uint_as_float(w[i]), __uint_as_float(w[i + 1]));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) A = absmax_nan(A, __shfl_xor_sync(kFull, A, o));
+    if (lane == 0) s_am[b][warp] = A;
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(32 * kQuadWarps) : "memory");
+#pragma unroll
+    for (int i = 0; i < kQuadWarps; ++i) A = absmax_nan(A, s_am[b][grp * kQuadWarps + i]);
+    float s = __fdiv_rn(A, Fmt8<FMT>::kMax);  // alpha / qmax
+    if (s == 0.0f) s = 1.0f;
+    const float r = __frcp_rn(s);
+    const bool fast = fast_div_ok(s);
+    if (q == 0 && lane == 0) {
+      a.scales[row] = s;
+      if (!is_finite_f(A)) flag_status(a.ws, QZ_FLAG_NONFINITE_INPUT);
+    }
+    const uint64_t r2 = pk(r, r), ns2 = pk(-s, -s), s2 = pk(s, s);
+    // pass 2: codes and statistics of the quarter, one chunk per lane per step
+    float tpart = 0.0f;
+    uint8_t* crow = a.codes + row * g.cols + static_cast<int64_t>(q) * cpq * EPC;
+#pragma unroll 1
+    for (int jb = 0; jb < cpq; jb += 32) {
+      const int j = jb + lane;
+      const bool valid = j < cpq;
+      uint32_t w[8];
+      if (valid) {
+        lds32B(w, slot + 32u * static_cast<uint32_t>(j));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = 0u;
+      }
+      if (acc.T >= 1.0f)
+        q8_chunk<FMT, DT, kTensorComputed, true, false, false>(w, valid, crow + static_cast<int64_t>(j) * EPC, s,
+                                                               r2, ns2, s2, z2, fast, a.ws, acc, tpart, am_unused);
+      else
+        q8_chunk<FMT, DT, kTensorComputed, true, true, false>(w, valid, crow + static_cast<int64_t>(j) * EPC, s,
+                                                              r2, ns2, s2, z2, fast, a.ws, acc, tpart, am_unused);
+    }
+    acc_add_sum(acc, tpart);
+    __syncwarp();  // every lane is done with the slot before it is refilled
+  }
+  stats_finish(acc, a.ws, a.stats, static_cast<uint64_t>(g.rows * g.cols));
+}
+
 template <typename K>
 qz_status go(K kern, const Q8Args& args, int64_t work_ctas, cudaStream_t s) {
   const int grid = grid_for(reinterpret_cast<const void*>(kern), work_ctas, s);
@@ -771,6 +888,19 @@ qz_status run_row(const Q8Args& args, cudaStream_t s) {
     if (g.cpr <= 64) return go2(&quant8_rowwarp_kernel<FMT, DT, STATS, 2>, args, work, s);
     if (g.cpr <= 128) return go2(&quant8_rowwarp_kernel<FMT, DT, STATS, 4>, args, work, s);
     return go2(&quant8_rowwarp_kernel<FMT, DT, STATS, 8>, args, work, s);
+  }
+  // with statistics, rows of whole chunks whose chunk count is a multiple of 4: four warps
+  // per row, double-buffered quarter rows
+  if (STATS && g.vec && row_bytes <= kRowQuadMaxBytes && row_bytes % (32 * kQuadWarps) == 0 &&
+      reinterpret_cast<uintptr_t>(args.x) % 16 == 0 && (g.ld * Elem<DT>::kBytes) % 16 == 0) {
+    auto kern = &quant8_rowquad_kernel<FMT, DT>;
+    const uint32_t slot = static_cast<uint32_t>((row_bytes / kQuadWarps + 127) / 128 * 128);
+    const size_t smem = static_cast<size_t>(kWarps) * 2 * slot;
+    if (!set_dyn_smem(reinterpret_cast<const void*>(kern), static_cast<int>(smem))) return QZ_ERR_CUDA;
+    const int grid = grid_for(reinterpret_cast<const void*>(kern), (rows + kWarps / kQuadWarps - 1) / (kWarps / kQuadWarps),
+                              s, smem);
+    kern<<<grid, kThreads, smem, s>>>(args, 0.0f, slot);
+    return launch_status();
   }
   // with statistics, rows of whole chunks up to 16 KiB: a warp and a shared-memory slot per row
   if (STATS && g.vec && row_bytes <= kRowSlotMaxBytes && row_bytes % 32 == 0 &&
