@@ -318,12 +318,14 @@ def test_named_workload_full_size(k):
 @pytest.mark.parametrize("fmt", FMT8)
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_parity_row_with_stats_paths(fmt, dtype):
-    """Per-row scales with the fused statistics: rows of whole chunks up to 16 KiB take a
-    warp and a shared-memory slot each; longer rows the row pipeline.  One-chunk rows, many
-    short rows, rows of exactly 16 KiB and just past it, and an odd row count."""
+    """Per-row scales with the fused statistics: rows of a multiple of 4 whole chunks up to
+    48 KiB take four warps each (a quarter row apiece); other rows of whole chunks up to
+    16 KiB a warp and a shared-memory slot each; longer rows the row pipeline.  One-chunk
+    rows, many short rows, rows of exactly 16 KiB and just past it, an odd row count, a
+    single row of whole quarters, and rows of 32 and 48 KiB."""
     eb = 2 if dtype == "bf16" else 4
     shapes = [(1, 32 // eb), (3000, 64), (77, 4096 + 32), (9, 16384 // eb), (5, 16384 // eb + 32 // eb),
-              (131, 1024)]
+              (131, 1024), (1, 2048 // eb), (2, 32768 // eb), (7, 49152 // eb)]
     for i, (r, c) in enumerate(shapes):
         x = gen(r, c, dtype, seed=1100 + i, kind="edge" if (dtype == "f32" and i % 2) else "lognormal")
         assert_parity(run_gpu(x, fmt, O.GRAN_ROW), run_oracle(x, fmt, O.GRAN_ROW))

@@ -92,6 +92,21 @@ def test_round_trip_without_stats():
                                    for k, t in h.items() if t is not None and k != "stats")
 
 
+def test_round_trip_int4_unit_and_row_scales():
+    """Scale layouts the other cases leave out: INT4 groups of 32 (fp32 scales per group),
+    MXFP4 and NVFP4 UNIT (scale bytes of value 1 per block), E5M2 ROW; fp32 input and f32
+    dequantized outputs, a ragged last chunk."""
+    from precision_quantization_gb300.streamed import HostRoundTrip
+    runs = [(O.INT4, O.GRAN_BLOCK), (O.MXFP4, O.GRAN_UNIT), (O.NVFP4, O.GRAN_UNIT), (O.E5M2, O.GRAN_ROW)]
+    rows, cols = 203, 512
+    x_np = W.lognormal_signed(rows, cols, seed=45, dtype="f32")
+    plan = HostRoundTrip(rows, cols, runs, in_dtype="f32", chunk_rows=64, out_dtype="f32")
+    plan.run(host_tensor(x_np))
+    for j, (f, g) in enumerate(runs):
+        check_run(plan, j, x_np, f, g)
+    assert plan.status() == 0
+
+
 def test_round_trip_pageable_input():
     """A host tensor that is not page-locked: the copies do not overlap, the results are
     the same."""
