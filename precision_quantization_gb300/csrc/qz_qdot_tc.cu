@@ -24,7 +24,7 @@
 //                 boundary (and every 1024 values of a longer group), commits each stage's
 //                 completion to the "empty" barriers of both rings (after the next stage's
 //                 first MMA) and each finished group to "P full".
-//   decoders      warps 2, 3, 4 and 6 (groups of 128 and more; one weight row per thread)
+//   decoders      warps 2, 3, 4 and 6 (groups of 64 and more; one weight row per thread)
 //                 or warps 2 and 3 (shorter groups; two rows per thread), never a warp on
 //                 the MMA warp's scheduler (w % 4 == 1).  Each thread copies its rows'
 //                 code words itself (cp.async, kRawAhead stages ahead), turns every word
@@ -240,11 +240,11 @@ struct Cursor {
   }
 };
 
-// DEC decoder warps: four for groups of 128 and more (measured when introduced, 4096^3 at
-// group 128: 345 -> 296 us); with their 768 threads (80 registers each) the epilogue's 64
-// accumulators spill a little, which costs more than the extra decoders gain when every
-// 16 to 64 values end a group (then: group 32 467 -> 715 us, group 64 392 -> 407 us), so
-// those run with two (640 threads, 96 registers).
+// DEC decoder warps: four for groups of 64 and more (4096^3: group 128 345 -> 296 us when
+// introduced; group 64 282 -> 264 us once the decode was straight-line); with their 768
+// threads (80 registers each) the epilogue's 64 accumulators spill a little, which costs
+// more than the extra decoders gain when every 16 or 32 values end a group (group 32:
+// 348 -> 445 us), so those run with two (640 threads, 96 registers).
 //
 // GW: code words per group when a stage's groups sit at fixed places in it -- 8 for every
 // group that is a multiple of 64 values (a stage lies inside one group), 4 for groups of
@@ -746,7 +746,7 @@ qz_status launch_quant_dot_tc(const uint32_t* w, const float* scales, const uint
   p.slice_stages = static_cast<int>(slice_stages);
   p.stages_total = static_cast<int>(stages_total);
   p.items = static_cast<int>(items);
-  const bool four = group >= 128;
+  const bool four = group >= 64;
   const int gw = group % 64 == 0 ? 8 : group == 32 ? 4 : group == 16 ? 2 : 0;
   void (*kern)(TcParams);
   if (four) kern = gw == 8 ? &quant_dot_tc_kernel<4, 8> : &quant_dot_tc_kernel<4, 0>;
