@@ -128,9 +128,21 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t adesc, uint64_t bdes
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc ? 1u : 0u)
       : "memory");
 }
-// 8 consecutive fp32 columns of this thread's tensor-memory lane, as 4 fp32 pairs (the
-// operands of the packed FMAs of the epilogue; 8 columns at a time keep the epilogue's
-// registers within the 80 a thread has)
+// 16 consecutive fp32 columns of this thread's tensor-memory lane, as 8 fp32 pairs (the
+// operands of the packed FMAs of the epilogue)
+__device__ __forceinline__ void tmem_ld16_pairs(uint32_t taddr, uint64_t (&v)[8]) {
+  asm volatile(
+      "{\n\t.reg .b32 r<16>;\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {r0,r1,r2,r3,r4,r5,r6,r7,r8,r9,r10,r11,r12,r13,r14,r15}, [%8];\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n\t"
+      "mov.b64 %0, {r0, r1};\n\tmov.b64 %1, {r2, r3};\n\tmov.b64 %2, {r4, r5};\n\tmov.b64 %3, {r6, r7};\n\t"
+      "mov.b64 %4, {r8, r9};\n\tmov.b64 %5, {r10, r11};\n\tmov.b64 %6, {r12, r13};\n\tmov.b64 %7, {r14, r15};\n\t}"
+      : "=l"(v[0]), "=l"(v[1]), "=l"(v[2]), "=l"(v[3]), "=l"(v[4]), "=l"(v[5]), "=l"(v[6]), "=l"(v[7])
+      : "r"(taddr)
+      : "memory");
+}
+// 8 consecutive fp32 columns, as 4 fp32 pairs (keeps the four-decoder kernel's epilogue
+// within the 80 registers a thread has there)
 __device__ __forceinline__ void tmem_ld8_pairs(uint32_t taddr, uint64_t (&v)[4]) {
   asm volatile(
       "{\n\t.reg .b32 r<8>;\n\t"
@@ -255,6 +267,9 @@ template <int DEC, int GW>
 __global__ void __launch_bounds__(TcShape<DEC>::kThreads, 1) quant_dot_tc_kernel(const __grid_constant__ TcParams p) {
   constexpr int kDecWarps = TcShape<DEC>::kDecWarps, kDecRows = TcShape<DEC>::kDecRows;
   constexpr int kFirstEpi = TcShape<DEC>::kFirstEpi;
+  // tensor-memory columns per epilogue load: 16 with the 96 registers of the two-decoder
+  // layout (half the load waits), 8 within the 80 of the four-decoder one
+  constexpr int kLdCols = DEC == 2 ? 16 : 8;
   extern __shared__ uint8_t tc_smem_raw[];
   __shared__ __align__(8) uint64_t yfull_bar[kYStages], yempty_bar[kYStages];
   __shared__ __align__(8) uint64_t afull_bar[kAStages], aempty_bar[kAStages];
@@ -614,11 +629,12 @@ __global__ void __launch_bounds__(TcShape<DEC>::kThreads, 1) quant_dot_tc_kernel
         tc_fence_after();
         const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(buf * kBN + 64 * cq);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {  // z = fl32(sc * P + z) for each element, two per FMA
-          uint64_t v[4];
-          tmem_ld8_pairs(ta + 8u * c, v);
+        for (int c = 0; c < 64 / kLdCols; ++c) {  // z = fl32(sc * P + z) for each element, two per FMA
+          uint64_t v[kLdCols / 2];
+          if constexpr (kLdCols == 16) tmem_ld16_pairs(ta + 16u * c, v);
+          else tmem_ld8_pairs(ta + 8u * c, v);
 #pragma unroll
-          for (int i = 0; i < 4; ++i) z2[4 * c + i] = fma2(v[i], sc2, z2[4 * c + i]);
+          for (int i = 0; i < kLdCols / 2; ++i) z2[(kLdCols / 2) * c + i] = fma2(v[i], sc2, z2[(kLdCols / 2) * c + i]);
         }
         tc_fence_before();
         __syncwarp();
