@@ -102,7 +102,9 @@ struct TcParams {
   float* z;
   int64_t ld_z;
   int n0, n1, mid, group, ng, sw;
-  int tiles_n, ksplit, slice_stages, stages_total, items;
+  // items [0, n_full) are whole tiles 0 .. n_full - 1; every later tile is split along l
+  // into ksplit slices of slice_stages stages (the last one shorter), one item each
+  int tiles_n, n_full, ksplit, slice_stages, stages_total, items;
 };
 
 // ---- small PTX wrappers -----------------------------------------------------------------
@@ -207,13 +209,21 @@ struct Item {
   int m0, nb, st0, nst;  // first weight row, first column, first stage, stages
   int nslab;             // 64-column boxes of y that hold columns < n1 (1 .. 4)
 };
+// Item `it` is one slice of several (its outputs are added into z).
+__device__ __forceinline__ bool item_split(const TcParams& p, int it) { return it >= p.n_full && p.ksplit > 1; }
 __device__ __forceinline__ Item item_of(const TcParams& p, int it) {
   Item r;
-  const int s = it % p.ksplit, t = it / p.ksplit;
+  int t = it, s = 0;
+  if (it >= p.n_full) {
+    const int j = it - p.n_full;
+    t = p.n_full + j / p.ksplit;
+    s = j % p.ksplit;
+  }
+  const bool split = item_split(p, it);
   r.m0 = (t / p.tiles_n) * kBM;
   r.nb = (t % p.tiles_n) * kBN;
-  r.st0 = s * p.slice_stages;
-  r.nst = min(p.slice_stages, p.stages_total - r.st0);
+  r.st0 = split ? s * p.slice_stages : 0;
+  r.nst = split ? min(p.slice_stages, p.stages_total - r.st0) : p.stages_total;
   r.nslab = min(4, (p.n1 - r.nb + 63) / 64);
   return r;
 }
@@ -648,13 +658,14 @@ __global__ void __launch_bounds__(TcShape<DEC>::kThreads, 1) quant_dot_tc_kernel
       }
       if (!ok) break;
       if (row_ok) {
+        const bool split = item_split(p, it);  // recomputed here: one register less in the loop
         const int c0 = I.nb + 64 * cq;
         float* zr = p.z + static_cast<int64_t>(row) * p.ld_z + c0;
         const int nv = min(64, p.n1 - c0);
         if (nv == 64 && zvec) {  // 16-byte stores (or reductions): 64 contiguous bytes a pair
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
-            if (p.ksplit > 1) red_pairs(zr + 2 * i, z2[i], z2[i + 1]);
+            if (split) red_pairs(zr + 2 * i, z2[i], z2[i + 1]);
             else st_pairs(zr + 2 * i, z2[i], z2[i + 1]);
           }
         } else {
@@ -662,7 +673,7 @@ __global__ void __launch_bounds__(TcShape<DEC>::kThreads, 1) quant_dot_tc_kernel
           for (int i = 0; i < 32; ++i) {
             float z0, z1;
             upk(z2[i], z0, z1);
-            if (p.ksplit > 1) {
+            if (split) {
               if (2 * i < nv) atomicAdd(zr + 2 * i, z0);
               if (2 * i + 1 < nv) atomicAdd(zr + 2 * i + 1, z1);
             } else {
@@ -739,12 +750,21 @@ qz_status launch_quant_dot_tc(const uint32_t* w, const float* scales, const uint
   const int sms = sm_count();
   const int64_t tiles_m = (n0 + kBM - 1) / kBM, tiles_n = (n1 + kBN - 1) / kBN;
   const int64_t tiles = tiles_m * tiles_n, stages_total = mid / kBK;
-  // split l when the tiles alone leave SMs idle, keeping slices of at least 256 values
+  // The whole waves of tiles run as they are; the tiles of the last, partly filled wave (all
+  // of them when there are fewer tiles than SMs) are split along l into as many slices as
+  // keep one slice per SM (k = floor(sms / tail)), of at least 256 values each, so that
+  // wave takes 1/k of a tile's time.  Measured against splitting only when there are fewer
+  // tiles than SMs (then into ceil(sms / tiles) slices): 4096^3 at groups of 128 (512
+  // tiles, 56 in the last wave, k = 2) 228 -> 215 us, groups of 32 342 -> 312 us,
+  // 32768 x 8192 x 2048 1436 -> 1409 us, 4096 x 4096 x 512 (64 tiles, k = 2 instead of 3)
+  // 57 -> 43 us.
+  const int64_t tail = tiles % sms;
   int64_t ksplit = 1;
-  if (tiles < sms) ksplit = std::max<int64_t>(1, std::min<int64_t>((sms + tiles - 1) / tiles, stages_total / 4));
+  if (tail > 0) ksplit = std::max<int64_t>(1, std::min<int64_t>(sms / tail, stages_total / 4));
   const int64_t slice_stages = (stages_total + ksplit - 1) / ksplit;
   ksplit = (stages_total + slice_stages - 1) / slice_stages;
-  const int64_t items = tiles * ksplit;
+  const int64_t n_full = ksplit > 1 ? tiles - tail : tiles;
+  const int64_t items = n_full + (tiles - n_full) * ksplit;
   if (items >= (int64_t{1} << 31)) return QZ_ERR_UNSUPPORTED;
   p.w = w;
   p.scales = scales;
@@ -758,6 +778,7 @@ qz_status launch_quant_dot_tc(const uint32_t* w, const float* scales, const uint
   p.ng = static_cast<int>(mid / group);
   p.sw = static_cast<int>((mid / group + 7) / 8);
   p.tiles_n = static_cast<int>(tiles_n);
+  p.n_full = static_cast<int>(n_full);
   p.ksplit = static_cast<int>(ksplit);
   p.slice_stages = static_cast<int>(slice_stages);
   p.stages_total = static_cast<int>(stages_total);
@@ -771,7 +792,10 @@ qz_status launch_quant_dot_tc(const uint32_t* w, const float* scales, const uint
   else if (gw == 2) kern = &quant_dot_tc_kernel<2, 2>;
   else kern = &quant_dot_tc_kernel<2, 0>;
   if (!set_dyn_smem(reinterpret_cast<const void*>(kern), static_cast<int>(kSmemTc))) return QZ_ERR_CUDA;
-  if (ksplit > 1 && launch_zero_z(z, ld_z, n0, n1, s) != QZ_OK) return QZ_ERR_CUDA;
+  if (ksplit > 1) {  // the split tiles add into z: zero their rows (from the first split tile's)
+    const int64_t row0 = (n_full / tiles_n) * kBM;
+    if (launch_zero_z(z + row0 * ld_z, ld_z, n0 - row0, n1, s) != QZ_OK) return QZ_ERR_CUDA;
+  }
   const int grid = static_cast<int>(std::min<int64_t>(items, sms));
   kern<<<grid, four ? TcShape<4>::kThreads : TcShape<2>::kThreads, kSmemTc, s>>>(p);
   return launch_status();

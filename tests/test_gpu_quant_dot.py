@@ -170,3 +170,27 @@ def test_quant_dot_many_columns_full_size_sampled(n0, mid, group, n1):
     got = z[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()].cpu().numpy()
     tol = qdot_tolerance(mid, group, za)
     assert np.all(np.abs(got.astype(np.float64) - zr) <= tol)
+
+
+def test_quant_dot_many_columns_split_last_wave():
+    """More tiles than SMs (154 tiles of 128 x 256 on a 152-SM GB300): the whole waves run as
+    they are, and the tiles of the last, partly filled wave are split along l and added into
+    z, which the library zeroes from the first split tile's row on.  Tile row 21 holds both
+    whole tiles (stored) and split ones (added), and z starts as a sentinel.  Exact sums, so
+    every sampled output must equal the oracle's bit for bit: the first rows, the last two
+    tile rows whole, and every third column with the last."""
+    import precision_quantization_gb300 as qz
+    torch = torch_mod()
+    n0, mid, group, n1 = 22 * 128 - 50, 1024, 128, 7 * 256 - 10
+    w, sc, sh, y = make_exact(n0, mid, group, n1, seed=1050)
+    zb = torch.full((n0, n1), 7.0, dtype=torch.float32, device="cuda")
+    z = qz.quant_dot(torch.from_numpy(w.view(np.int32)).cuda(), torch.from_numpy(sc).cuda(),
+                     torch.from_numpy(sh.view(np.int32)).cuda(), group,
+                     torch.from_numpy(y.view(np.int16)).cuda().view(torch.bfloat16), out=zb)
+    torch.cuda.synchronize()
+    rows = np.concatenate([np.arange(6), np.arange(20 * 128, n0)])
+    cols = np.unique(np.concatenate([np.arange(0, n1, 3), [n1 - 1]]))
+    zr, _ = O.quant_dot(w[rows], sc[rows], sh[rows], np.ascontiguousarray(y[:, cols]), group)
+    got = z[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()].cpu().numpy()
+    bad = np.argwhere(got.astype(np.float64) != zr)
+    assert bad.size == 0, (len(bad), tuple(bad[0]))
